@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark: µs per routed-expert MoE layer and weight-byte HBM GB/s on one GB300.
+
+One step = one whole MoE layer on the device: route (expert-major row lists) -> gate/up rows
+(+ SwiGLU + E4M3 quantiser) -> down rows -> combine, four launches of libtfx_moe.so on one
+stream. Default workload: the DeepSeek-class 1-row decode layer (H 7168, I 2048, 256 experts,
+top-8, E4M3 activations, MXFP4 weights), synthetic and seeded. Inputs are resident in HBM
+before the timed region; each step uses the next of 4 packed layer copies (different expert
+weights), so 4 x 187 MB of distinct weights rotate and no step finds the last one's in L2.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle instead (the only
+reference this method has), on a bounded sample per step, scaled to µs per layer.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per MoE layer and weight-byte HBM GB/s vs peak at R=1..16 rows"
+UNIT = "us per MoE layer"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def expert_bytes(H, I):
+    """Codes + scales of one expert's gate, up and down projections."""
+    return 3 * I * (H // 2) + 3 * I * (H // 32)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "shared", "apart", "chunk"])
+    ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for n in ("tfx_rows.cu", "tfx_common.cuh"):
+        with open(os.path.join(ROOT, "moe_routed_expert_major_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, R):
+    """dram bytes (read + write) per gate/up launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "upc_rows_%s_r%d.md" % (workload, R))
+    if not os.path.exists(p):
+        return None
+    src = None
+    traffic = None
+    for line in open(p):
+        if line.startswith("kernel_source_hash:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("dram_bytes_per_launch:"):
+            traffic = float(line.split(":", 1)[1].strip())
+    return traffic if src == kernel_hash() else None
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [t.strip() for t in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, fl in rows for i, v in enumerate(fl) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------ ours
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import synth
+    from moe_routed_expert_major_gb300 import build as _build
+    from moe_routed_expert_major_gb300 import tfx
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    _build.build()
+    tfx.load()
+
+    over = {} if args.rows is None else {"R": args.rows}
+    cfg = synth.workload(args.workload, **over)
+    H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
+    d = tfx.dims(H, I, E, k)
+    inp = synth.make_inputs(cfg)
+    if kind == synth.ACT_E4M3:
+        x = torch.from_numpy(inp["x"]).to(dev)
+        xs = torch.from_numpy(inp["sx"]).to(dev)
+    else:
+        x = torch.from_numpy(inp["x"].view(np.int16)).to(dev)
+        xs = None
+    ids = torch.from_numpy(inp["ids"]).to(dev)
+    w = torch.from_numpy(inp["w"]).to(dev)
+    L = max(1, args.layers)
+    packed = []
+    for l in range(L):
+        dw = synth.weights_torch(E, H, I, cfg["seed"] + 7919 * l, dev)
+        p = torch.empty(tfx.tfx_xp_packed_bytes(d), dtype=torch.uint8, device=dev)
+        tfx.tfx_xp_pack(d, dw, p)
+        packed.append(p)
+        del dw
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    buf = tfx.alloc_layer(R, H, I, E, k, kind, dev)
+    n_distinct = len(set(int(e) for e in inp["ids"].ravel()))
+    wbytes = n_distinct * expert_bytes(H, I)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        pk = packed[i % L]
+        tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
+        if ev is not None:
+            ev[0].record(stream)
+        tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+        if ev is not None:
+            ev[1].record(stream)
+        tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if int(buf["status"].item()) != 0:
+        raise RuntimeError("device status %d during warm-up" % int(buf["status"].item()))
+
+    # ---------------------------------------------------------------- timed region
+    K = args.steps
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clk = Clocks(local)
+    clk.start()
+    time.sleep(0.25)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(K):
+        step(i, kev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = clk.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    upc_ms = [a.elapsed_time(b) for a, b in kev]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = int(buf["status"].item())
+
+    # per-kernel breakdown (diagnostic, outside the timed region)
+    names = ["route", "upc_rows", "down_rows", "combine"]
+    nb = min(200, K)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
+    for i in range(nb):
+        pk = packed[i % L]
+        e = evs[i]
+        e[0].record(stream)
+        tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
+        e[1].record(stream)
+        tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+        e[2].record(stream)
+        tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        e[3].record(stream)
+        tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
+        e[4].record(stream)
+    torch.cuda.synchronize()
+    breakdown = {n: 1000.0 * statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nb))
+                 for j, n in enumerate(names)}
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(inp["x"] if kind == synth.ACT_E4M3 else inp["x"].view(np.int16)).pin_memory()
+        hxs = torch.from_numpy(inp["sx"]).pin_memory() if kind == synth.ACT_E4M3 else None
+        hids = torch.from_numpy(inp["ids"]).pin_memory()
+        hw = torch.from_numpy(inp["w"]).pin_memory()
+        hy = torch.empty(buf["y"].shape, dtype=buf["y"].dtype).pin_memory()
+        dx, dxs, dids, dwt = torch.empty_like(x), (torch.empty_like(xs) if xs is not None else None), torch.empty_like(ids), torch.empty_like(w)
+        h2d = hx.numel() * hx.element_size() + (hxs.numel() if hxs is not None else 0) + hids.numel() * 4 + hw.numel() * 4
+        d2h = hy.numel() * hy.element_size()
+        Ke = min(K, 2000)
+
+        def e2e_step(i):
+            dx.copy_(hx, non_blocking=True)
+            if dxs is not None:
+                dxs.copy_(hxs, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            dwt.copy_(hw, non_blocking=True)
+            pk = packed[i % L]
+            tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
+            tfx.tfx_xp_upc_rows(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+            tfx.tfx_xp_combine(d, R, buf["out"], dwt, buf["y"])
+            hy.copy_(buf["y"], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(Ke):
+            e2e_step(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e = {"value": 1000.0 * a.elapsed_time(b) / Ke, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+
+    # ---------------------------------------------------------------- CPU oracle baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_full_layer(cfg, inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds)
+
+    hbm, hbm_src = peaks()
+    upc_avg_ms = statistics.fmean(upc_ms)
+    P = R * k
+    upc_alg = n_distinct * 2 * I * (H // 2 + H // 32) + R * (H + (H // 32 if kind == synth.ACT_E4M3 else H)) \
+        + P * (I + I // 32 if kind == synth.ACT_E4M3 else 2 * I)
+    achieved = upc_alg / (upc_avg_ms * 1e-3) / 1e9
+    us_per_layer = 1000.0 * elapsed_ms / (K * world)
+    line = {
+        "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s: H %d, I %d, E %d, top-%d, R %d, %s activations, MXFP4 weights" % (
+            args.workload, H, I, E, k, R, "E4M3" if kind == synth.ACT_E4M3 else "bf16"),
+            "rows": R, "distinct_experts": n_distinct, "weight_bytes_per_layer": wbytes,
+            "layers_rotated": L, "l2": "inputs larger than L2: %d packed layer copies rotate (%.0f MB of distinct "
+                                        "weights per rotation vs 129 MB L2)" % (L, L * wbytes / 1e6),
+            "parallelism": "replicas" if world > 1 else "single GPU"},
+        "weight_gbs": round(wbytes / (us_per_layer * 1e-6) / 1e9, 1),
+        "weight_gbs_frac_of_peak": round(wbytes / (us_per_layer * 1e-6) / 1e9 / hbm, 4),
+        "kernels_us": {n: round(v, 3) for n, v in breakdown.items()},
+        "roofline": {"kernel": "upc_rows", "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_source": hbm_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "algorithmic_bytes_per_launch": int(upc_alg), "avg_launch_us": round(1000 * upc_avg_ms, 3),
+                     "traffic": profiled_traffic(args.workload, R)},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K, "clocks": clocks, "status": status,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _host_layer(cfg, inp, dev):
+    import synth
+    dw = synth.weights_torch(cfg["E"], cfg["H"], cfg["I"], cfg["seed"], dev)
+    experts = sorted(set(int(e) for e in inp["ids"].ravel()))
+    lay = dict(H=cfg["H"], I=cfg["I"], E=cfg["E"], k=cfg["k"], kind=cfg["kind"])
+    for n, t in dw.items():
+        full = {}
+        for e in experts:
+            full[e] = t[e].cpu().numpy()
+        lay[n] = _ExpertDict(full)
+    lay.update(inp)
+    return lay
+
+
+class _ExpertDict:
+    def __init__(self, d):
+        self.d = d
+
+    def __getitem__(self, e):
+        return self.d[int(e)]
+
+
+def cpu_baseline_full_layer(cfg, inp, packed_seed, dev, seconds):
+    """The oracle (fp32-chain mode, as it stands) on whole layers of the same workload."""
+    import oracle
+    lay = _host_layer(cfg, inp, dev)
+    R, k = inp["ids"].shape
+    threads = min(os.cpu_count() or 1, R * k)
+    oracle.layer_chain(lay, threads=threads, rows=[0])  # load and warm the library
+    n = 0
+    t = time.perf_counter()
+    while True:
+        oracle.layer_chain(lay, threads=threads)
+        n += 1
+        el = time.perf_counter() - t
+        if el >= seconds or n >= 50:
+            break
+    return {"value": round(1e6 * el / n, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d whole %s layer(s) (route, %d gate/up + SwiGLU + quantiser + down pairs, combine), "
+                      "fp32-chain mode, pairs spread over %d host threads" % (n, cfg["name"], R * k, threads)}
+
+
+# ------------------------------------------------------------------------------- reference
+
+def run_reference(args):
+    """The CPU oracle timed on the host cores: each step computes a bounded sample of the
+    layer (gate/up for 8 outputs and down for 16 outputs of one (row, slot) pair, rotating
+    over the pairs), and the time is scaled to a whole layer by the share of multiply-adds."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    over = {} if args.rows is None else {"R": args.rows}
+    cfg = synth.workload(args.workload, **over)
+    H, I, k, R, kind = cfg["H"], cfg["I"], cfg["k"], cfg["R"], cfg["kind"]
+    inp = synth.make_inputs(cfg)
+    dev = "cuda:0" if torch.cuda.is_available() else "cpu"
+    lay = _host_layer(cfg, inp, dev)
+    rt = oracle.route(inp["ids"], cfg["E"])
+    P = len(rt["pair_row"])
+    # unscaled activation values and group scales, decoded by the oracle's own element formats
+    e4 = np.array([oracle.e4m3_value(c) for c in range(256)], np.float32)
+
+    def act(r):
+        if kind == synth.ACT_E4M3:
+            xc = e4[inp["x"][r]]
+            xs = np.array([oracle.ue8m0_value(int(s)) for s in inp["sx"][r]], np.float32)
+        else:
+            xc = oracle.bf16_to_f32(inp["x"][r])
+            xs = np.ones(H // 32, np.float32)
+        return np.ascontiguousarray(xc), xs
+
+    acts = {r: act(r) for r in set(int(r) for r in rt["pair_row"])}
+    hc = np.ones(I, np.float32)
+    hsc = np.ones(I // 32, np.float32)
+    NG, ND = 8, 16
+
+    def one(i):
+        p = i % P
+        r, j = int(rt["pair_row"][p]), int(rt["pair_slot"][p])
+        e = int(inp["ids"][r, j])
+        xc, xs = acts[r]
+        for q in range(NG):
+            n = (i * NG + q) % I
+            oracle.chain_dot(lay["wg"][e][n], lay["sg"][e][n], xc, xs)
+            oracle.chain_dot(lay["wu"][e][n], lay["su"][e][n], xc, xs)
+        for q in range(ND):
+            m = (i * ND + q) % H
+            oracle.chain_dot(lay["wd"][e][m], lay["sd"][e][m], hc, hsc)
+
+    for i in range(args.warmup):
+        one(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    el = time.perf_counter() - t
+    frac = (NG * 2 * H + ND * I) / float(P * 3 * H * I)
+    us = 1e6 * (el / args.steps) / frac
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * el / args.steps, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s: H %d, I %d, E %d, top-%d, R %d, %s activations, MXFP4 weights" % (
+                args.workload, H, I, cfg["E"], k, R, "E4M3" if kind == synth.ACT_E4M3 else "bf16"), "rows": R},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "per step: gate/up for %d outputs and down for %d outputs of one routed pair "
+                                       "(fp32-chain mode, one thread), scaled by multiply-adds to a whole layer of "
+                                       "%d pairs" % (NG, ND, P)},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

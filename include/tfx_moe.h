@@ -1,0 +1,175 @@
+/*
+ * tfx_moe.h -- C ABI of the GB300 routed-expert MoE library (libtfx_moe.so, sm_103a).
+ *
+ * The library computes the routed-expert part of a DeepSeek-style MoE layer over
+ * block-scaled FP4 weights for a launch of R token rows:
+ *   route:    top-k expert ids [R][k] -> expert-major row lists (each expert's rows)
+ *   upc_rows: per routed (row, slot) pair, g = x.Wg_e, u = x.Wu_e, h = silu(g) * u,
+ *             h quantised to the launch's activation format
+ *   down_rows: d[row][slot] = h . Wd_e
+ *   combine:  y[row] = sum over slots (in slot order) of w[row][slot] * d[row][slot], bf16
+ * Source of the method: "dsv41 metal: decode experts decode an expert's weights once for all
+ * of its rows" (TensorFold PR #2983): "What this changes" and the commit message of the
+ * rows kernels (tf_dsv41_xp_upc_rows / tf_dsv41_xp_down_rows, passes sized by the rows
+ * left, padding rows computed and never written, the combine output checked per row).
+ *
+ * Numbers and formats
+ *   Weights: MXFP4 (OCP MX v1.0): E2M1 codes, two per byte, the lower k in the low nibble,
+ *   one E8M0 scale (2^(s-127), 0xFF = NaN) per 32 consecutive k of one output row.
+ *   Activations: E4M3 (OCP OFP8, no infinities, 0x7F/0xFF NaN) with one E8M0 scale per 32
+ *   consecutive k (TFX_ACT_E4M3), or bf16 (TFX_ACT_BF16).
+ *   Accumulators (g, u, d) follow one fixed fp32 order for every row, whatever else is in
+ *   the launch ("What this changes": each row's 32 products run as a sequential fma chain
+ *   from zero in k order, then the scaled fma, then the eight-way tree):
+ *     for each 32-group G:  p = fma chain of the 32 unscaled products, from +0, k ascending
+ *                           acc[G mod 8] = fma(p, 2^(sw-127) * 2^(sx-127), acc[G mod 8])
+ *     result = ((acc0+acc4) + (acc2+acc6)) + ((acc1+acc5) + (acc3+acc7))
+ *   so every row's g, u and d are bit-identical alone or with any other rows and routing.
+ *   Epilogue: h = (g / (1 + exp(-g))) * u in fp32. E4M3 launches quantise h per 32
+ *   consecutive outputs with the OCP MX rule (shared exponent floor(log2 amax) - 8, nearest
+ *   even, saturating at 448; amax 0 -> scale code 127; NaN/Inf in the block -> scale 0xFF
+ *   and NaN codes). bf16 launches round h to bf16 (nearest even).
+ *   Combine: y = fma chain over the k slots in slot order from +0, then bf16 (nearest even).
+ *
+ * Conventions
+ *   Every pointer is a DEVICE pointer owned by the caller unless stated. The library never
+ *   allocates, frees, synchronises or keeps a pointer after a call returns; every call is
+ *   asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream).
+ *   Return value: TFX_OK, or a negative TFX_E* found before anything was launched.
+ *   Faults found on the device are OR-ed into the caller's `status` word (int32, device
+ *   memory; TFX_ST_* bits), which the caller reads after its own synchronisation; the
+ *   library never clears it. A pair whose expert id is out of range or repeats an earlier
+ *   slot's id in the same row is left out of every list and its outputs are not written.
+ *   Waits inside the kernels are bounded: a wait that runs out sets TFX_ST_TIMEOUT and the
+ *   kernel returns early (outputs then incomplete).
+ *   R = 0 is a no-op returning TFX_OK.
+ */
+#ifndef TFX_MOE_H
+#define TFX_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes */
+#define TFX_OK 0
+#define TFX_EINVAL (-1)       /* null/misaligned pointer, negative or inconsistent sizes */
+#define TFX_EUNSUPPORTED (-2) /* shape the kernels do not cover (see each entry point) */
+#define TFX_ELAUNCH (-3)      /* the CUDA launch itself failed */
+#define TFX_ECUDA (-4)        /* a CUDA query (device, attributes) failed */
+
+#define TFX_ST_RANGE 1   /* an expert id was outside [0, E) */
+#define TFX_ST_DUP 2     /* an expert id repeated an earlier slot of the same row */
+#define TFX_ST_TIMEOUT 4 /* a bounded wait ran out; the kernel stopped early */
+#define TFX_ST_SHAPE 8   /* route data inconsistent with the launch (corrupt lists) */
+
+#define TFX_ACT_E4M3 0 /* E4M3 codes [rows][K] + E8M0 scales [rows][K/32] */
+#define TFX_ACT_BF16 1 /* bf16 [rows][K] */
+
+typedef struct {
+  int32_t hidden;    /* H: model width; multiple of 64 */
+  int32_t inter;     /* I: expert intermediate width; multiple of 32 */
+  int32_t n_experts; /* E: routed experts; 1..1024 */
+  int32_t top_k;     /* k: experts per row; 1..32 and <= E */
+} tfx_dims;
+
+/* Expert-major row lists written by tfx_xp_route (all device pointers).
+ *   offs      [E+1]  pairs of expert e are offs[e] .. offs[e+1]-1
+ *   pair_row  [R*k]  token row of each pair, ascending (row, slot) within an expert
+ *   pair_slot [R*k]  slot (0..k-1) of each pair
+ *   active    [min(R*k, E)]  experts with at least one pair, ascending id
+ *   n_active  [1]    number of entries in active */
+typedef struct {
+  const int32_t* offs;
+  const int32_t* pair_row;
+  const int32_t* pair_slot;
+  const int32_t* active;
+  const int32_t* n_active;
+} tfx_route;
+
+/* Optional knobs of the rows kernels (pass NULL for the defaults). None changes a bit of
+ * any output; they exist for tuning and for the tests that prove it.
+ *   max_pass  largest pass (rows decoded against one read of the weights): 0 = automatic
+ *             from R; else 1, 2, 4 or 8 (gate/up) and 1, 2 or 4 (down).
+ *   tier_mode 0 = pass sized by the rows left as on the pages (gate/up 8 if >= 7 rows
+ *             left, 6 if >= 5, 4 if >= 3, else 2 or 1; down 4 if >= 3, else 2 or 1);
+ *             1 = every pass at max_pass (padding rows repeat the last real row, are
+ *             computed and never written).
+ *   timeout_ns bound of every wait; 0 = 2 s. */
+typedef struct {
+  int32_t max_pass;
+  int32_t tier_mode;
+  int64_t timeout_ns;
+} tfx_rows_opts;
+
+/* ---------------------------------------------------------------- weights
+ * The rows kernels read the experts' weights in a packed device layout that puts each
+ * CTA's stage of codes and scales in one contiguous block, so that one bulk copy fetches
+ * it. tfx_xp_pack converts the canonical layout once (at load time):
+ *   wg, wu: codes [E][I][H/2], sg, su: scales [E][I][H/32]   (gate and up projections)
+ *   wd: codes [E][H][I/2], sd: scales [E][H][I/32]           (down projection)
+ * into `packed` (tfx_xp_packed_bytes(d) bytes, 16-byte aligned). Packed layout: for each
+ * expert, for each block of 32 outputs n of I, for each stage of 512 k: 64 rows (32 gate
+ * rows, then the 32 up rows of the same n) of 256 code bytes, then those 64 rows' 16
+ * scale bytes; after all experts' gate/up, the same for the down projection with blocks of
+ * 64 outputs m of H. k beyond H (or I) in the last stage is zero-filled.
+ * Returns TFX_EINVAL for null pointers or bad dims. */
+size_t tfx_xp_packed_bytes(tfx_dims d);
+int tfx_xp_pack(tfx_dims d, const uint8_t* wg, const uint8_t* sg, const uint8_t* wu, const uint8_t* su,
+                const uint8_t* wd, const uint8_t* sd, uint8_t* packed, void* stream);
+
+/* ---------------------------------------------------------------- route
+ * Builds the expert-major row lists ("every expert's rows", #2983 commit message) from
+ * ids [R][k] (int32, row-major). Pairs of one expert are in ascending (row, slot) order;
+ * active experts in ascending id. Invalid ids set TFX_ST_RANGE / TFX_ST_DUP in *status and
+ * are left out. Output buffers: offs [E+1], pair_row and pair_slot [R*k],
+ * active [min(R*k, E)], n_active [1]. E must be <= 1024. */
+int tfx_xp_route(tfx_dims d, int32_t rows, const int32_t* ids, int32_t* offs, int32_t* pair_row,
+                 int32_t* pair_slot, int32_t* active, int32_t* n_active, int32_t* status, void* stream);
+
+/* ---------------------------------------------------------------- gate/up rows
+ * For every routed pair p (expert-major order of `rt`), with row r = pair_row[p]:
+ *   g = x[r] . Wg_e, u = x[r] . Wu_e (fp32 chains above), h = silu(g) * u,
+ * written as h[p][0..I) in the launch's activation format:
+ *   TFX_ACT_E4M3: x = E4M3 codes [R][H] + x_scale E8M0 [R][H/32]; h = E4M3 codes [R*k][I]
+ *                 + h_scale [R*k][I/32]
+ *   TFX_ACT_BF16: x = bf16 [R][H] (x_scale NULL); h = bf16 [R*k][I] (h_scale NULL)
+ * Each expert's weights are read once per pass for all of the pass's rows ("decode each
+ * 32-group of an expert's MXFP4 weights once per pass and apply it to every row in it").
+ * Optional debug outputs (NULL to skip): gu_dbg fp32 [R*k][2][I] (g then u), h_dbg fp32
+ * [R*k][I] (h before quantisation). x, h and packed must be 16-byte aligned. */
+int tfx_xp_upc_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                    const uint8_t* x_scale, const tfx_route* rt, void* h, uint8_t* h_scale, float* gu_dbg,
+                    float* h_dbg, int32_t* status, const tfx_rows_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------- down rows
+ * For every routed pair p: out[pair_row[p]][pair_slot[p]][0..H) = h[p] . Wd_e (fp32 chain).
+ * h and h_scale as written by tfx_xp_upc_rows; out is fp32 [R][k][H]. Entries of pairs
+ * that were left out (invalid ids) are not written. */
+int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* h,
+                     const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
+                     const tfx_rows_opts* opts, void* stream);
+
+/* ---------------------------------------------------------------- combine
+ * y[r][m] = fma chain over j = 0..k-1 of topk_w[r][j] * out[r][j][m] from +0, rounded to
+ * bf16 (nearest even). out fp32 [R][k][H], topk_w fp32 [R][k], y bf16 bits [R][H],
+ * y_f32_dbg fp32 [R][H] or NULL. */
+int tfx_xp_combine(tfx_dims d, int32_t rows, const float* out, const float* topk_w, uint16_t* y,
+                   float* y_f32_dbg, void* stream);
+
+/* ---------------------------------------------------------------- misc */
+const char* tfx_strerror(int code);
+int tfx_version(void);
+
+/* Self-test of the bounded wait: launches one block that waits on a barrier nothing will
+ * complete, with the given limit in nanoseconds; the wait runs out, TFX_ST_TIMEOUT is OR-ed
+ * into *status and the kernel returns. */
+int tfx_selftest_wait_timeout(int32_t* status, int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,136 @@
+// tfx_route.cu -- expert-major row lists ("every expert's rows", commit message of the rows
+// kernels in TensorFold PR #2983): a stable counting sort of the (row, slot) pairs by expert
+// id, in one CTA of 1024 threads.
+//
+// The pairs are split into 32 contiguous chunks, one per warp. Phase 1: each warp counts its
+// chunk per expert (shared-memory histogram [32][E]). Phase 2: per expert, exclusive sums
+// over the warps and over the experts give each (warp, expert) its first position, the
+// offsets and the active list. Phase 3: each warp walks its chunk in rounds of 32 pairs; a
+// pair's position is its (warp, expert) base plus its rank among the round's pairs of the
+// same expert (__match_any_sync), so every expert's pairs come out in ascending
+// (row, slot) order whatever the thread timing.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tfx_common.cuh"
+
+namespace tfx {
+
+constexpr int RT_THREADS = 1024;
+constexpr int RT_WARPS = RT_THREADS / 32;
+
+// A pair is valid if its id is in range and no earlier slot of its row has the same id.
+__device__ __forceinline__ int pair_expert(const int32_t* ids, int q, int k, int E, int* bad) {
+  const int e = ids[q];
+  if (e < 0 || e >= E) { *bad |= TFX_ST_RANGE; return -1; }
+  const int r0 = q - q % k;
+  for (int jj = r0; jj < q; ++jj)
+    if (ids[jj] == e) { *bad |= TFX_ST_DUP; return -1; }
+  return e;
+}
+
+__global__ void __launch_bounds__(RT_THREADS) route_kernel(const int32_t* __restrict__ ids, int P, int k, int E,
+                                                           int32_t* offs, int32_t* pair_row, int32_t* pair_slot,
+                                                           int32_t* active, int32_t* n_active, int32_t* status) {
+  extern __shared__ int hist[];  // [RT_WARPS][E], then scan scratch [E]
+  int* eoff = hist + RT_WARPS * E;
+  __shared__ int s_bad;
+  __shared__ int s_nact;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < RT_WARPS * E; i += RT_THREADS) hist[i] = 0;
+  if (tid == 0) { s_bad = 0; s_nact = 0; }
+  __syncthreads();
+
+  const int chunk = (P + RT_WARPS - 1) / RT_WARPS;
+  const int c0 = min(P, warp * chunk), c1 = min(P, c0 + chunk);
+  int bad = 0;
+  // phase 1: per-warp histogram
+  for (int q = c0 + lane; q < c1; q += 32) {
+    const int e = pair_expert(ids, q, k, E, &bad);
+    if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
+  }
+  if (bad) atomicOr(&s_bad, bad);
+  __syncthreads();
+
+  // phase 2: per expert, exclusive sum over warps; then over experts (serial per block of 32
+  // experts a warp, then a scan of the block totals by warp 0)
+  for (int e = tid; e < E; e += RT_THREADS) {
+    int run = 0;
+    for (int w = 0; w < RT_WARPS; ++w) {
+      const int c = hist[w * E + e];
+      hist[w * E + e] = run;
+      run += c;
+    }
+    eoff[e] = run;  // total of expert e for now
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int base = 0, abase = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int c = e < E ? eoff[e] : 0;
+      int inc = c, act = (c > 0) ? 1 : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, o);
+        const int a = __shfl_up_sync(0xffffffffu, act, o);
+        if (lane >= o) { inc += v; act += a; }
+      }
+      if (e < E) {
+        const int start = base + inc - c;
+        eoff[e] = start;
+        offs[e] = start;
+        if (c > 0) active[abase + act - 1] = e;
+      }
+      base += __shfl_sync(0xffffffffu, inc, 31);
+      abase += __shfl_sync(0xffffffffu, act, 31);
+    }
+    if (lane == 0) {
+      offs[E] = base;
+      s_nact = abase;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    *n_active = s_nact;
+    if (s_bad && status) atomicOr(status, s_bad);
+  }
+
+  // phase 3: stable scatter
+  for (int q0 = c0; q0 < c1; q0 += 32) {
+    const int q = q0 + lane;
+    int dummy = 0;
+    const int e = q < c1 ? pair_expert(ids, q, k, E, &dummy) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int leader = __ffs(peers) - 1;
+    if (e >= 0) {
+      const int pos = eoff[e] + hist[warp * E + e] + rank;
+      pair_row[pos] = q / k;
+      pair_slot[pos] = q % k;
+    }
+    __syncwarp();
+    if (e >= 0 && lane == leader) hist[warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+}  // namespace tfx
+
+using namespace tfx;
+
+extern "C" int tfx_xp_route(tfx_dims d, int32_t rows, const int32_t* ids, int32_t* offs, int32_t* pair_row,
+                            int32_t* pair_slot, int32_t* active, int32_t* n_active, int32_t* status, void* stream) {
+  if (d.n_experts < 1 || d.n_experts > 1024 || d.top_k < 1 || d.top_k > 32 || rows < 0) return TFX_EINVAL;
+  if ((int64_t)rows * d.top_k > (1ll << 30)) return TFX_EINVAL;
+  if (!offs || !active || !n_active || !status) return TFX_EINVAL;
+  if (rows > 0 && (!ids || !pair_row || !pair_slot)) return TFX_EINVAL;
+  const int E = d.n_experts;
+  const size_t smem = (size_t)(RT_WARPS + 1) * E * sizeof(int);
+  auto kern = route_kernel;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return TFX_ELAUNCH;
+  kern<<<1, RT_THREADS, smem, static_cast<cudaStream_t>(stream)>>>(ids, rows * d.top_k, d.top_k, E, offs, pair_row,
+                                                                 pair_slot, active, n_active, status);
+  return cudaGetLastError() == cudaSuccess ? TFX_OK : TFX_ELAUNCH;
+}

@@ -1,0 +1,72 @@
+"""The C-ABI library builds for sm_103a, loads, exports every function include/tfx_moe.h
+declares, and rejects bad arguments before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tfx_moe.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(tfx_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+        pytest.skip("nvcc not available")
+    from moe_routed_expert_major_gb300 import build, tfx
+    build.build()
+    return tfx.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("tfx_xp_route", "tfx_xp_upc_rows", "tfx_xp_down_rows", "tfx_xp_combine", "tfx_xp_pack",
+              "tfx_xp_packed_bytes", "tfx_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_packed_size(lib):
+    from moe_routed_expert_major_gb300 import tfx
+    # 256 experts x (22,020,096 code bytes + 1,376,256 scale bytes): no padding at these widths
+    assert tfx.tfx_xp_packed_bytes(tfx.dims(7168, 2048, 256, 8)) == 256 * 23396352
+    assert tfx.tfx_xp_packed_bytes(tfx.dims(100, 2048, 256, 8)) == 0   # H not a multiple of 64
+
+
+def test_invalid_arguments_are_rejected_before_launch(lib):
+    from moe_routed_expert_major_gb300 import tfx
+    d = tfx.dims(7168, 2048, 256, 8)
+    bad = tfx.dims(7168, 2048, 0, 8)
+    st = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    rt = tfx.Route(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16))
+    L = lib
+    assert L.tfx_xp_route(bad, 1, st, st, st, st, st, st, st, None) == -1
+    assert L.tfx_xp_route(d, -1, st, st, st, st, st, st, st, None) == -1
+    assert L.tfx_xp_route(d, 1, None, st, st, st, st, st, st, None) == -1
+    # upc: null packed, misaligned x, bad kind, bad max_pass
+    assert L.tfx_xp_upc_rows(d, 1, 0, None, st, st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
+    assert L.tfx_xp_upc_rows(d, 1, 0, st, ctypes.c_void_p(17), st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
+    assert L.tfx_xp_upc_rows(d, 1, 7, st, st, st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
+    o = tfx.opts_struct(max_pass=3)
+    assert L.tfx_xp_upc_rows(d, 1, 0, st, st, st, ctypes.byref(rt), st, st, None, None, st, ctypes.byref(o), None) == -1
+    o = tfx.opts_struct(max_pass=8)
+    assert L.tfx_xp_down_rows(d, 1, 0, st, st, st, ctypes.byref(rt), st, st, ctypes.byref(o), None) == -1
+    assert L.tfx_xp_down_rows(d, 1, 0, st, st, st, None, st, st, None, None) == -1
+    assert L.tfx_xp_combine(tfx.dims(100, 2048, 256, 8), 1, st, st, st, None, None) == -1
+    assert L.tfx_xp_combine(d, 1, None, st, st, None, None) == -1
+    assert L.tfx_xp_pack(bad, st, st, st, st, st, st, st, None) == -1
+    assert L.tfx_selftest_wait_timeout(None, 1000, None) == -1
+    assert L.tfx_strerror(-2) == b"unsupported shape for these kernels"
