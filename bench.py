@@ -2,8 +2,8 @@
 """Benchmark: µs per routed-expert MoE layer and weight-byte HBM GB/s on one GB300.
 
 One step = one whole MoE layer on the device: route (expert-major row lists) -> gate/up rows
-(+ SwiGLU + E4M3 quantiser) -> down rows -> combine, four launches of libtfx_moe.so on one
-stream. Default workload: the DeepSeek-class 1-row decode layer (H 7168, I 2048, 256 experts,
+(+ SwiGLU + E4M3 quantiser) -> down rows -> combine, in one launch of libtfx_moe.so
+(tfx_xp_moe_rows; --path separate times the four separate launches instead). Default workload: the DeepSeek-class 1-row decode layer (H 7168, I 2048, 256 experts,
 top-8, E4M3 activations, MXFP4 weights), synthetic and seeded. Inputs are resident in HBM
 before the timed region; each step uses the next of 4 packed layer copies (different expert
 weights), so 4 x 187 MB of distinct weights rotate and no step finds the last one's in L2.
@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "shared", "apart", "chunk"])
     ap.add_argument("--rows", type=int, default=None)
     ap.add_argument("--layers", type=int, default=4)
+    ap.add_argument("--experts", type=int, default=None, help="override E (profiling aid: same widths, less memory)")
+    ap.add_argument("--eager", action="store_true", help="launch each step from Python instead of graph replay")
+    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
+                    help="fused: one launch per layer (tfx_xp_moe_rows); separate: route, gate/up, down, combine")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -70,10 +74,10 @@ def kernel_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, R):
-    """dram bytes (read + write) per gate/up launch from the committed ncu summary, if it was
-    taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "upc_rows_%s_r%d.md" % (workload, R))
+def profiled_traffic(workload, R, kernel):
+    """dram bytes (read + write) per launch of the timed kernel from the committed ncu summary,
+    if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "%s_rows_%s_r%d.md" % (kernel, workload, R))
     if not os.path.exists(p):
         return None
     src = None
@@ -154,6 +158,8 @@ def run_ours(args):
     tfx.load()
 
     over = {} if args.rows is None else {"R": args.rows}
+    if args.experts is not None:
+        over["E"] = args.experts
     cfg = synth.workload(args.workload, **over)
     H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
     d = tfx.dims(H, I, E, k)
@@ -181,14 +187,25 @@ def run_ours(args):
     wbytes = n_distinct * expert_bytes(H, I)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    fused = args.path == "fused" and R * k <= 256
+
+    def step(i, ev=None, st=None):
         pk = packed[i % L]
+        st = stream if st is None else st
+        if fused:
+            if ev is not None:
+                ev[0].record(st)
+            tfx.tfx_xp_moe_rows(d, R, kind, pk, x, xs, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
+                                buf["y"], buf["scratch"], buf["status"])
+            if ev is not None:
+                ev[1].record(st)
+            return
         tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
         if ev is not None:
-            ev[0].record(stream)
+            ev[0].record(st)
         tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
         if ev is not None:
-            ev[1].record(stream)
+            ev[1].record(st)
         tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
         tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
 
@@ -199,8 +216,35 @@ def run_ours(args):
         raise RuntimeError("device status %d during warm-up" % int(buf["status"].item()))
 
     # ---------------------------------------------------------------- timed region
+    # Steps are replayed from a CUDA graph (G steps cycling over the layer copies, with timing
+    # events around every timed kernel captured as graph nodes), so the host's launch rate does
+    # not shape the device timeline; --eager launches every step from Python instead.
     K = args.steps
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    G = 8 * L
+    graph = None
+    kev = None
+    if not args.eager:
+        try:
+            kev = [(torch.cuda.Event(enable_timing=True, external=True),
+                    torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
+            graph = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                with torch.cuda.graph(graph, stream=cs):
+                    for i in range(G):
+                        step(i, kev[i], torch.cuda.current_stream())
+            torch.cuda.synchronize()
+            for _ in range(2):
+                graph.replay()
+            torch.cuda.synchronize()
+        except (TypeError, RuntimeError) as ex:  # no graph timing events in this torch: eager
+            sys.stderr.write("graph capture unavailable (%s); timing eager launches\n" % ex)
+            graph = None
+    if graph is not None:
+        K = max(G, (K + G - 1) // G * G)
+    else:
+        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     clk = Clocks(local)
@@ -210,15 +254,19 @@ def run_ours(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0.record(stream)
-    for i in range(K):
-        step(i, kev[i])
+    if graph is not None:
+        for _ in range(K // G):
+            graph.replay()
+    else:
+        for i in range(K):
+            step(i, kev[i])
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = clk.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    upc_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
     if world > 1:
         t = torch.tensor([elapsed_ms], dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -265,10 +313,14 @@ def run_ours(args):
             dids.copy_(hids, non_blocking=True)
             dwt.copy_(hw, non_blocking=True)
             pk = packed[i % L]
-            tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
-            tfx.tfx_xp_upc_rows(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
-            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
-            tfx.tfx_xp_combine(d, R, buf["out"], dwt, buf["y"])
+            if fused:
+                tfx.tfx_xp_moe_rows(d, R, kind, pk, dx, dxs, dids, dwt, buf["route"], buf["h"], buf["h_scale"],
+                                    buf["out"], buf["y"], buf["scratch"], buf["status"])
+            else:
+                tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
+                tfx.tfx_xp_upc_rows(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+                tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+                tfx.tfx_xp_combine(d, R, buf["out"], dwt, buf["y"])
             hy.copy_(buf["y"], non_blocking=True)
 
         for i in range(3):
@@ -289,11 +341,20 @@ def run_ours(args):
         cpu = cpu_baseline_full_layer(cfg, inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds)
 
     hbm, hbm_src = peaks()
-    upc_avg_ms = statistics.fmean(upc_ms)
+    kern_avg_ms = statistics.fmean(kern_ms)
     P = R * k
-    upc_alg = n_distinct * 2 * I * (H // 2 + H // 32) + R * (H + (H // 32 if kind == synth.ACT_E4M3 else H)) \
-        + P * (I + I // 32 if kind == synth.ACT_E4M3 else 2 * I)
-    achieved = upc_alg / (upc_avg_ms * 1e-3) / 1e9
+    act_b = 1 if kind == synth.ACT_E4M3 else 2
+    x_b = R * H * act_b + (R * (H // 32) if kind == synth.ACT_E4M3 else 0)
+    h_b = P * I * act_b + (P * (I // 32) if kind == synth.ACT_E4M3 else 0)
+    if fused:
+        # weights of the distinct experts once, activations in, h written and read back, the
+        # expert outputs written and read back by the combine, ids/weights, and y
+        kern_name = "moe_rows (route+gate/up+down+combine, one launch)"
+        kern_alg = wbytes + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
+    else:
+        kern_name = "upc_rows"
+        kern_alg = n_distinct * 2 * I * (H // 2 + H // 32) + x_b + h_b
+    achieved = kern_alg / (kern_avg_ms * 1e-3) / 1e9
     us_per_layer = 1000.0 * elapsed_ms / (K * world)
     line = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -304,15 +365,17 @@ def run_ours(args):
             "rows": R, "distinct_experts": n_distinct, "weight_bytes_per_layer": wbytes,
             "layers_rotated": L, "l2": "inputs larger than L2: %d packed layer copies rotate (%.0f MB of distinct "
                                         "weights per rotation vs 129 MB L2)" % (L, L * wbytes / 1e6),
+            "path": "fused one-launch layer" if fused else "route + gate/up + down + combine",
             "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": round(wbytes / (us_per_layer * 1e-6) / 1e9, 1),
         "weight_gbs_frac_of_peak": round(wbytes / (us_per_layer * 1e-6) / 1e9 / hbm, 4),
-        "kernels_us": {n: round(v, 3) for n, v in breakdown.items()},
-        "roofline": {"kernel": "upc_rows", "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+        "separate_kernels_us": {n: round(v, 3) for n, v in breakdown.items()},
+        "roofline": {"kernel": kern_name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": hbm_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "algorithmic_bytes_per_launch": int(upc_alg), "avg_launch_us": round(1000 * upc_avg_ms, 3),
-                     "traffic": profiled_traffic(args.workload, R)},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 4 * K, "clocks": clocks, "status": status,
+                     "algorithmic_bytes_per_launch": int(kern_alg), "avg_launch_us": round(1000 * kern_avg_ms, 3),
+                     "traffic": profiled_traffic(args.workload, R, "fused" if fused else "upc")},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 4) * K, "clocks": clocks,
+        "status": status, "launch": "cuda graph replay" if graph is not None else "eager",
     }
     if rank == 0:
         print(json.dumps(line))

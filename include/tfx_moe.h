@@ -153,6 +153,30 @@ int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* 
                      const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
                      const tfx_rows_opts* opts, void* stream);
 
+/* ---------------------------------------------------------------- whole layer, one launch
+ * Route, gate/up, down and combine of a small launch (R*k <= 256 routed pairs: decode) in a
+ * single kernel launch, with the same results, bit for bit, as tfx_xp_route followed by
+ * tfx_xp_upc_rows, tfx_xp_down_rows and tfx_xp_combine. Every CTA builds the row lists in
+ * shared memory (the first also writes them to offs .. n_active, sized as for tfx_xp_route);
+ * down items wait (bounded) for their expert's gate/up items; each (row, 64-output block) is
+ * combined by the CTA whose down item writes the row's last valid slot. Rows with a left-out
+ * slot (invalid id) get no combine output.
+ * ids int32 [R][k], topk_w fp32 [R][k]; h / h_scale / out as for the separate entries; y bf16
+ * [R][H]; y_f32_dbg fp32 [R][H] or NULL.
+ * scratch: tfx_xp_moe_rows_scratch_bytes(d, R) bytes of device memory, 4-byte aligned, zero
+ * before its first use; every call returns it to zero, so calls sharing one scratch buffer
+ * must not overlap on the device. The CTAs of one launch wait on one another, so the launch
+ * is cooperative (all CTAs resident at once; the runtime refuses it otherwise: TFX_ELAUNCH);
+ * a wait that runs out sets TFX_ST_TIMEOUT.
+ * Returns TFX_EUNSUPPORTED for R*k > 256. opts->max_pass applies to gate/up (1, 2, 4 or 8);
+ * the down pass is the same capped at 4. */
+size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows);
+int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                    const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
+                    int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
+                    uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
+                    int32_t* status, const tfx_rows_opts* opts, void* stream);
+
 /* ---------------------------------------------------------------- combine
  * y[r][m] = fma chain over j = 0..k-1 of topk_w[r][j] * out[r][j][m] from +0, rounded to
  * bf16 (nearest even). out fp32 [R][k][H], topk_w fp32 [R][k], y bf16 bits [R][H],

@@ -58,6 +58,9 @@ def load():
             "tfx_xp_down_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, ctypes.POINTER(Route), _P, _P,
                                                 ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_combine": (ctypes.c_int, [Dims, _I32, _P, _P, _P, _P, _P]),
+            "tfx_xp_moe_rows_scratch_bytes": (ctypes.c_size_t, [Dims, _I32]),
+            "tfx_xp_moe_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                               _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "tfx_version": (ctypes.c_int, []),
             "tfx_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
@@ -137,6 +140,19 @@ def tfx_xp_combine(d, rows, out, topk_w, y, y_f32=None):
            "tfx_xp_combine")
 
 
+def tfx_xp_moe_rows_scratch_bytes(d, rows):
+    return int(load().tfx_xp_moe_rows_scratch_bytes(d, rows))
+
+
+def tfx_xp_moe_rows(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, h, h_scale, out, y, scratch, status,
+                    y_f32=None, opts=None):
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(load().tfx_xp_moe_rows(d, rows, kind, _ptr(packed), _ptr(x), _ptr(x_scale), _ptr(ids), _ptr(topk_w),
+                                  _ptr(rt["offs"]), _ptr(rt["pair_row"]), _ptr(rt["pair_slot"]), _ptr(rt["active"]),
+                                  _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out), _ptr(y), _ptr(y_f32),
+                                  _ptr(scratch), _ptr(status), o, _stream()), "tfx_xp_moe_rows")
+
+
 def tfx_selftest_wait_timeout(status, timeout_ns):
     _check(load().tfx_selftest_wait_timeout(_ptr(status), int(timeout_ns), _stream()), "tfx_selftest_wait_timeout")
 
@@ -162,6 +178,8 @@ def alloc_layer(R, H, I, E, k, kind, device, debug=False):
         b["h_scale"] = None
     b["out"] = torch.empty(max(R, 1), k, H, dtype=torch.float32, device=device)
     b["y"] = torch.empty(max(R, 1), H, dtype=torch.int16, device=device)
+    nsc = tfx_xp_moe_rows_scratch_bytes(Dims(H, I, E, k), max(R, 1)) // 4
+    b["scratch"] = torch.zeros(max(nsc, 1), dtype=torch.int32, device=device)
     if debug:
         b["gu_dbg"] = torch.empty(P, 2, I, dtype=torch.float32, device=device)
         b["h_dbg"] = torch.empty(P, I, dtype=torch.float32, device=device)
@@ -169,6 +187,12 @@ def alloc_layer(R, H, I, E, k, kind, device, debug=False):
     else:
         b["gu_dbg"] = b["h_dbg"] = b["y_f32"] = None
     return b
+
+
+def layer_fused(d, R, kind, packed, x, x_scale, ids, w, buf, opts=None):
+    """One MoE layer of R rows in a single launch (tfx_xp_moe_rows)."""
+    tfx_xp_moe_rows(d, R, kind, packed, x, x_scale, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
+                    buf["y"], buf["scratch"], buf["status"], buf["y_f32"], opts)
 
 
 def layer_rows(d, R, kind, packed, x, x_scale, ids, w, buf, opts_upc=None, opts_down=None):

@@ -122,3 +122,44 @@ def bf16_equal(a, b):
     fa = (np.asarray(a).view(np.uint16).astype(np.uint32) << 16).view(np.float32)
     fb = (np.asarray(b).view(np.uint16).astype(np.uint32) << 16).view(np.float32)
     return bits_equal(fa, fb)
+
+
+def run_layer_fused(lay, packed, opts=None, canary=None, scratch=None):
+    """The whole layer in one launch (tfx_xp_moe_rows); returns numpy results and the scratch."""
+    R, k = lay["ids"].shape
+    d = tfx.dims(lay["H"], lay["I"], lay["E"], k)
+    xd, xs, ids, w = to_dev_inputs(lay)
+    buf = tfx.alloc_layer(R, lay["H"], lay["I"], lay["E"], k, lay["kind"], DEV, debug=True)
+    if scratch is not None:
+        buf["scratch"] = scratch
+    if canary is not None:
+        for n in ("h", "h_scale", "out", "y", "y_f32"):
+            if buf.get(n) is not None:
+                buf[n].view(torch.uint8).fill_(canary)
+    tfx.layer_fused(d, R, lay["kind"], packed, xd, xs, ids, w, buf, opts)
+    torch.cuda.synchronize()
+    res = {n: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for n, v in buf.items() if n != "route"}
+    res["route"] = {n: v.cpu().numpy() for n, v in buf["route"].items()}
+    res["status"] = int(buf["status"].item())
+    return res, buf["scratch"]
+
+
+def assert_same_layer(a, b, lay, rows=None):
+    """Fused and separate launches: identical row lists, h, d and combine output."""
+    R, k = lay["ids"].shape
+    n = int(a["route"]["offs"][-1])
+    assert np.array_equal(a["route"]["offs"], b["route"]["offs"])
+    assert np.array_equal(a["route"]["pair_row"][:n], b["route"]["pair_row"][:n])
+    assert np.array_equal(a["route"]["pair_slot"][:n], b["route"]["pair_slot"][:n])
+    assert int(a["route"]["n_active"][0]) == int(b["route"]["n_active"][0])
+    assert np.array_equal(a["h"][:n].view(np.uint8), b["h"][:n].view(np.uint8))
+    if a["h_scale"] is not None:
+        assert np.array_equal(a["h_scale"][:n], b["h_scale"][:n])
+    routed = set(zip(a["route"]["pair_row"][:n].tolist(), a["route"]["pair_slot"][:n].tolist()))
+    rows = range(R) if rows is None else rows
+    for r in rows:
+        for j in range(k):
+            if (r, j) in routed:
+                assert np.array_equal(a["out"][r, j].view(np.uint32), b["out"][r, j].view(np.uint32)), (r, j)
+        assert np.array_equal(a["y"][r].view(np.uint16), b["y"][r].view(np.uint16)), r
+        assert np.array_equal(a["y_f32"][r].view(np.uint32), b["y_f32"][r].view(np.uint32)), r

@@ -1,0 +1,93 @@
+"""The one-launch layer (tfx_xp_moe_rows) against the four separate launches: identical row
+lists, h, d and combine output bit for bit, on small and full-width layers, every pass-size
+setting and the routing/NaN matrix; its scratch returns to zero after every call."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import gpu_util as gu  # noqa: E402
+from moe_routed_expert_major_gb300 import tfx  # noqa: E402
+from test_gpu_invariance import make_case, ROWS  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from moe_routed_expert_major_gb300 import build
+    build.build()
+    tfx.load()
+
+
+@pytest.mark.parametrize("kind", [synth.ACT_E4M3, synth.ACT_BF16], ids=["e4m3", "bf16"])
+@pytest.mark.parametrize("shape", [dict(H=256, I=128, E=8, k=2, R=4), dict(H=1088, I=96, E=16, k=4, R=7),
+                                   dict(H=2048, I=544, E=6, k=3, R=13), dict(H=512, I=64, E=40, k=8, R=32)],
+                         ids=["tiny", "ragged", "stages", "p256"])
+def test_fused_equals_separate(kind, shape):
+    cfg = synth.workload("tiny", kind=kind, seed=17, **{n: v for n, v in shape.items() if n != "R"})
+    lay = synth.make_layer_numpy(cfg, R=shape["R"])
+    d = tfx.dims(lay["H"], lay["I"], lay["E"], lay["ids"].shape[1])
+    packed = gu.pack(d, gu.device_weights_from_numpy(lay))
+    sep = gu.run_layer(lay, packed)
+    fus, scratch = gu.run_layer_fused(lay, packed)
+    assert sep["status"] == 0 and fus["status"] == 0
+    gu.assert_same_layer(fus, sep, lay)
+    assert int(scratch.abs().sum().item()) == 0
+    # a second call on the same scratch gives the same bits
+    fus2, _ = gu.run_layer_fused(lay, packed, scratch=scratch)
+    gu.assert_same_layer(fus2, sep, lay)
+    assert int(scratch.abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("kind", [synth.ACT_E4M3, synth.ACT_BF16], ids=["e4m3", "bf16"])
+def test_fused_matrix_and_pass_sizes(kind):
+    from test_gpu_invariance import H, I, E, K
+    lay0 = synth.make_layer_numpy(synth.workload("tiny", kind=synth.ACT_E4M3, H=H, I=I, E=E, k=K, seed=99), R=1)
+    d = tfx.dims(H, I, E, K)
+    packed = gu.pack(d, gu.device_weights_from_numpy(lay0))
+    for routing in ("same", "disjoint", "random"):
+        for planted in (False, True):
+            for R in ROWS:
+                lay = make_case(lay0, kind, routing, R, planted, seed=2000 + R)
+                sep = gu.run_layer(lay, packed, debug=True)
+                fus, _ = gu.run_layer_fused(lay, packed)
+                gu.assert_same_layer(fus, sep, lay)
+    lay = make_case(lay0, kind, "same", 16, False, seed=5)
+    sep = gu.run_layer(lay, packed, debug=True)
+    for mp in (1, 2, 4, 8):
+        for tm in (0, 1):
+            fus, _ = gu.run_layer_fused(lay, packed, opts=tfx.opts_struct(max_pass=mp, tier_mode=tm))
+            gu.assert_same_layer(fus, sep, lay)
+
+
+def test_fused_invalid_ids():
+    lay = synth.make_layer_numpy(synth.workload("tiny", kind=synth.ACT_E4M3, H=256, I=64, E=8, k=3, seed=5), R=5)
+    lay["ids"][1, 2] = 8
+    lay["ids"][3, 1] = lay["ids"][3, 0]
+    d = tfx.dims(256, 64, 8, 3)
+    packed = gu.pack(d, gu.device_weights_from_numpy(lay))
+    sep = gu.run_layer(lay, packed)
+    fus, scratch = gu.run_layer_fused(lay, packed, canary=0x33)
+    assert fus["status"] == tfx.ST_RANGE | tfx.ST_DUP
+    gu.assert_same_layer(fus, sep, lay, rows=[0, 2, 4])
+    assert np.all(fus["y"][1].view(np.uint8) == 0x33) and np.all(fus["y"][3].view(np.uint8) == 0x33)
+    assert int(scratch.abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("name,R", [("decode", 1), ("shared", 16), ("apart", 16)])
+def test_fused_full_width(name, R):
+    cfg = synth.workload(name)
+    lay, dw = gu.full_layer(cfg, R=R)
+    d = tfx.dims(cfg["H"], cfg["I"], cfg["E"], cfg["k"])
+    packed = gu.pack(d, dw)
+    del dw
+    sep = gu.run_layer(lay, packed)
+    fus, scratch = gu.run_layer_fused(lay, packed)
+    assert sep["status"] == 0 and fus["status"] == 0
+    gu.assert_same_layer(fus, sep, lay)
+    assert int(scratch.abs().sum().item()) == 0
