@@ -159,8 +159,9 @@ int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* 
  * tfx_xp_upc_rows, tfx_xp_down_rows and tfx_xp_combine. Every CTA builds the row lists in
  * shared memory (the first also writes them to offs .. n_active, sized as for tfx_xp_route);
  * down items wait (bounded) for their expert's gate/up items; each (row, 64-output block) is
- * combined by the CTA whose down item writes the row's last valid slot. Rows with a left-out
- * slot (invalid id) get no combine output.
+ * combined by the CTA whose down item writes the row's last valid slot. As with
+ * tfx_xp_combine, a row with a left-out slot (invalid id, flagged in status) combines that
+ * slot's unwritten (stale) entries of out.
  * ids int32 [R][k], topk_w fp32 [R][k]; h / h_scale / out as for the separate entries; y bf16
  * [R][H]; y_f32_dbg fp32 [R][H] or NULL.
  * scratch: tfx_xp_moe_rows_scratch_bytes(d, R) bytes of device memory, 4-byte aligned, zero
