@@ -178,6 +178,27 @@ int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* p
                     uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
                     int32_t* status, const tfx_rows_opts* opts, void* stream);
 
+/* The one-launch layer without caller scratch (no counterpart on the pages: it is an
+ * interface for callers that cannot allocate). Some callers cannot call cudaMalloc: code
+ * running inside a host runtime that owns every device allocation through its own pool, or
+ * a plugin on a path where an allocation would synchronise the device or fail. This entry
+ * point allocates nothing and calls no allocating routine: the completion counters live in a
+ * 64 KiB buffer compiled into the library (a file-scope __device__ array, held by every GPU
+ * that loads the library until the process exits), cleared on `stream` at the start of each
+ * call. Arguments and results are those of tfx_xp_moe_rows without `scratch`; the caller
+ * still passes every input and output buffer.
+ * Limit: tfx_xp_moe_rows_scratch_bytes(d, R) <= 65536 bytes (16,384 counters), else
+ * TFX_EUNSUPPORTED before anything is launched.
+ * The first call on a device looks up the buffer's device address (cudaGetSymbolAddress);
+ * make that first call before any stream capture on the device. Every call on a device
+ * shares the one buffer: calls that overlap on the GPU (other streams, other threads) race
+ * and give wrong results; serialise them. */
+int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                            const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
+                            int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
+                            uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* status,
+                            const tfx_rows_opts* opts, void* stream);
+
 /* ---------------------------------------------------------------- combine
  * y[r][m] = fma chain over j = 0..k-1 of topk_w[r][j] * out[r][j][m] from +0, rounded to
  * bf16 (nearest even). out fp32 [R][k][H], topk_w fp32 [R][k], y bf16 bits [R][H],

@@ -976,3 +976,59 @@ extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_FUSED>(P, mu, md, max_items, st);
   return dispatch<TFX_ACT_BF16, PH_FUSED>(P, mu, md, max_items, st);
 }
+
+// ------------------------------------------------------------------------------ no-alloc variant
+// The one-launch layer for callers that cannot allocate device memory themselves: its
+// completion counters live in a buffer compiled into the library instead of caller scratch.
+namespace tfx {
+
+// Capacity of the built-in counter buffer, in int32 words (64 KiB on every device that
+// loads the library, held until the process exits).
+constexpr int NOALLOC_SCRATCH_INTS = 16384;
+static __device__ __align__(256) int32_t g_noalloc_scratch[NOALLOC_SCRATCH_INTS];
+
+// Device address of g_noalloc_scratch per device, looked up once with that device current.
+// (In host code the array's name is only a host-side stand-in, never a device address.)
+static int32_t* g_noalloc_ptr[64];
+
+static int noalloc_scratch(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TFX_ECUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      (void)cudaGetLastError();
+      return TFX_ECUDA;
+    }
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return TFX_OK;
+}
+
+}  // namespace tfx
+
+extern "C" int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed,
+                                       const void* x, const uint8_t* x_scale, const int32_t* ids,
+                                       const float* topk_w, int32_t* offs, int32_t* pair_row, int32_t* pair_slot,
+                                       int32_t* active, int32_t* n_active, void* h, uint8_t* h_scale, float* out,
+                                       uint16_t* y, float* y_f32_dbg, int32_t* status, const tfx_rows_opts* opts,
+                                       void* stream) {
+  const size_t need = tfx_xp_moe_rows_scratch_bytes(d, rows) / sizeof(int32_t);
+  if (need > (size_t)NOALLOC_SCRATCH_INTS) return TFX_EUNSUPPORTED;  // beyond the built-in buffer
+  int32_t* scratch = nullptr;
+  if (need > 0 && rows > 0) {
+    const int rc = noalloc_scratch(&scratch);
+    if (rc) return rc;
+    // the counters must start at zero; a previous call on this device may have stopped early
+    if (cudaMemsetAsync(scratch, 0, need * sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return TFX_ELAUNCH;
+    }
+  } else {
+    scratch = reinterpret_cast<int32_t*>(16);  // never touched: zero rows or arguments rejected below
+  }
+  return tfx_xp_moe_rows(d, rows, act_kind, packed, x, x_scale, ids, topk_w, offs, pair_row, pair_slot, active,
+                         n_active, h, h_scale, out, y, y_f32_dbg, scratch, status, opts, stream);
+}

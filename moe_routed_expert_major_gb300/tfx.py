@@ -61,6 +61,8 @@ def load():
             "tfx_xp_moe_rows_scratch_bytes": (ctypes.c_size_t, [Dims, _I32]),
             "tfx_xp_moe_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
+            "tfx_xp_moe_rows_noalloc": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                       _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "tfx_version": (ctypes.c_int, []),
             "tfx_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
@@ -151,6 +153,17 @@ def tfx_xp_moe_rows(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, h, h_sca
                                   _ptr(rt["offs"]), _ptr(rt["pair_row"]), _ptr(rt["pair_slot"]), _ptr(rt["active"]),
                                   _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out), _ptr(y), _ptr(y_f32),
                                   _ptr(scratch), _ptr(status), o, _stream()), "tfx_xp_moe_rows")
+
+
+def tfx_xp_moe_rows_noalloc(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, h, h_scale, out, y, status,
+                            y_f32=None, opts=None):
+    """tfx_xp_moe_rows with the library's built-in counter buffer instead of caller scratch."""
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(load().tfx_xp_moe_rows_noalloc(d, rows, kind, _ptr(packed), _ptr(x), _ptr(x_scale), _ptr(ids),
+                                          _ptr(topk_w), _ptr(rt["offs"]), _ptr(rt["pair_row"]), _ptr(rt["pair_slot"]),
+                                          _ptr(rt["active"]), _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out),
+                                          _ptr(y), _ptr(y_f32), _ptr(status), o, _stream()),
+           "tfx_xp_moe_rows_noalloc")
 
 
 def tfx_selftest_wait_timeout(status, timeout_ns):
