@@ -44,9 +44,13 @@ constexpr int CODE_B = KC / 2;                   // code bytes per row per stage
 constexpr int STAGE_B = TROWS * (CODE_B + GPS);  // 17,408
 constexpr int NCW = 8;                           // consumer warps
 constexpr int NCONS = NCW * kWarp;               // 256
-constexpr int NTHREADS = NCONS + kWarp;          // + one producer warp
+constexpr int NTHREADS = NCONS + 3 * kWarp;      // + producer, stager and epilogue warps
+constexpr int W_PROD = NCW;                      // producer warp index (weight stages)
+constexpr int W_HELP = NCW + 1;                  // stager warp index (activation buffers)
+constexpr int W_EPI = NCW + 2;                   // epilogue warp index (results out)
 constexpr int MAX_NSTAGE = 8;
 constexpr int FUSED_MAX_PAIRS = 256;
+constexpr int QD = 4;                            // claimed-item queue depth (fused)
 
 enum { PH_UPC = 1, PH_DOWN = 2, PH_FUSED = 3 };
 
@@ -60,6 +64,10 @@ struct RowsParams {
   int H, I, E, k, R;
   Proj pu, pd;
   int nstage;
+  int nxb;              // activation buffers in shared memory (2: the next pass stages while this one runs)
+  int use_raw;          // 1: activation rows arrive by bulk copy into a shared-memory raw buffer
+  int raw_row, raw_sc;  // raw buffer bytes per row (128-aligned) and per row of scales (16-aligned)
+  int sc_tma_u, sc_tma_d;  // scales of gate/up (x) / down (h) rows come by bulk copy too
   int gbmax;            // group blocks allotted per activation row in shared memory
   int route_ints;       // shared-memory ints of the in-kernel route (fused)
   const void* x;        // token activations [R][H]
@@ -74,8 +82,8 @@ struct RowsParams {
   float* out;           // [R][k][H]
   uint16_t* y;          // fused: [R][H] bf16
   float* y32;           // fused: [R][H] or null
-  int32_t* scratch;     // fused: [0] exit count, [1..E] gate/up items done per active expert,
-                        //        then [R][H/64] slots written per (row, block)
+  int32_t* scratch;     // fused: [0] exit count, [1] work counter, [2..E+1] gate/up items done
+                        //        per active expert, then [R][H/64] slots written per (row, block)
   int32_t* status;
   int tier_mode;
   uint64_t timeout_ns;
@@ -83,19 +91,22 @@ struct RowsParams {
 
 // ---------------------------------------------------------------- shared-memory layout
 struct Layout {
-  int bars, ctrl, pass, epi, route, ring, xs, xm, total;
+  int bars, ctrl, pdesc, epi, route, ring, xs, xm, xs_stride, xm_stride, raw, total;
 };
 __host__ __device__ inline Layout layout_of(const RowsParams& p, int maxr) {
   Layout L;
-  L.bars = 0;      // full[8], empty[8]
-  L.ctrl = 128;    // abort flag
-  L.pass = 256;    // prow[8], ppair[8]
-  L.epi = 512;     // float [8][64]
-  L.route = 2560;  // fused: ints
+  L.bars = 0;      // full[8], empty[8], xfull[2], xempty[2], efull[2], eempty[2], rawfull, qfull[4], qempty[4]
+  L.ctrl = 384;    // abort flag, then the claimed-item queue ids
+  L.pdesc = 448;   // two pass descriptors: prow[8], ppair[8]
+  L.epi = 640;     // two float [8][64] result buffers
+  L.route = 4736;  // fused: ints
   L.ring = (L.route + 4 * p.route_ints + 127) & ~127;
   L.xs = L.ring + p.nstage * STAGE_B;
-  L.xm = L.xs + maxr * p.gbmax * 512;
-  L.total = L.xm + maxr * p.gbmax * 8 * 4;
+  L.xs_stride = maxr * p.gbmax * 512;
+  L.xm = L.xs + p.nxb * L.xs_stride;
+  L.xm_stride = maxr * p.gbmax * 8 * 4;
+  L.raw = (L.xm + p.nxb * L.xm_stride + 127) & ~127;
+  L.total = L.raw + (p.use_raw ? maxr * (p.raw_row + p.raw_sc) : 0);
   return L;
 }
 
@@ -135,30 +146,62 @@ __device__ __noinline__ float chain_bf16_exact(uint4 codes, const uint16_t* xrow
   return p;
 }
 
-// Stage the activation rows of one pass into shared memory (consumer threads only). Groups
-// from G up to the stage boundary are zero with multiplier 1, so that lanes past the end of
-// the reduction add +0 to their accumulators.
-template <int KIND>
-__device__ void stage_rows(const uint8_t* __restrict__ X8, const uint8_t* __restrict__ XS, int K, int G, int GB,
-                           uint8_t* xs_s, float* xm_s, const int* prow, int real, int tid) {
+// Stage the activation rows of one pass into the f16 activation buffer (the NT threads of the
+// calling role). Row r is read at X8 + row(r) * xstride and its scales at XS + row(r) * sstride,
+// where row(r) = prow[r] for rows in global memory, or r for rows already bulk-copied into
+// shared memory (FROM_SMEM). Global loads go through L2 (the rows may have been written by
+// other CTAs of the same launch) and are issued in batches so that many are in flight. Groups
+// from G up to the stage boundary are zero with multiplier 1, so that lanes past the end of the
+// reduction add +0 to their accumulators.
+template <int KIND, bool FROM_SMEM, bool SC_SMEM>
+__device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const uint8_t* __restrict__ XS,
+                           size_t sstride, int K, int G, int GB, uint8_t* xs_s, float* xm_s, const int* prow,
+                           int real, int tid, int NT) {
   const int nch = K / 8;          // chunks of 8 elements with data
   const int nall = GB * 8 * 4;    // chunks up to the stage boundary
+  constexpr int BATCH = 8;
   if (KIND == TFX_ACT_E4M3) {
-    for (int i = tid; i < real * nall; i += NCONS) {
-      const int r = i / nall, c = i - r * nall;
-      uint4 o = make_uint4(0u, 0u, 0u, 0u);
-      if (c < nch) {
-        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(X8 + (size_t)prow[r] * K + 8 * c));
-        o.x = e4m3x2_to_f16x2(v.x);
-        o.y = e4m3x2_to_f16x2(v.x >> 16);
-        o.z = e4m3x2_to_f16x2(v.y);
-        o.w = e4m3x2_to_f16x2(v.y >> 16);
+    const int gall = GB * 8;
+    for (int r = 0; r < real; ++r) {
+      const uint8_t* xrow = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride;
+      for (int c0 = tid; c0 < nall; c0 += BATCH * NT) {
+        uint2 v[BATCH];
+#pragma unroll
+        for (int q = 0; q < BATCH; ++q) {
+          const int c = c0 + q * NT;
+          v[q] = make_uint2(0u, 0u);
+          if (c < nch)
+            v[q] = FROM_SMEM ? *reinterpret_cast<const uint2*>(xrow + 8 * c)
+                             : __ldcg(reinterpret_cast<const uint2*>(xrow + 8 * c));
+        }
+#pragma unroll
+        for (int q = 0; q < BATCH; ++q) {
+          const int c = c0 + q * NT;
+          if (c >= nall) break;
+          uint4 o;
+          o.x = e4m3x2_to_f16x2(v[q].x);
+          o.y = e4m3x2_to_f16x2(v[q].x >> 16);
+          o.z = e4m3x2_to_f16x2(v[q].y);
+          o.w = e4m3x2_to_f16x2(v[q].y >> 16);
+          *reinterpret_cast<uint4*>(xs_s + xoff(r, c >> 2, c & 3, GB)) = o;
+        }
       }
-      *reinterpret_cast<uint4*>(xs_s + xoff(r, c >> 2, c & 3, GB)) = o;
-    }
-    for (int i = tid; i < real * GB * 8; i += NCONS) {
-      const int r = i / (GB * 8), g = i - r * (GB * 8);
-      xm_s[r * GB * 8 + g] = g < G ? e8m0_to_f32(__ldcg(XS + (size_t)prow[r] * G + g)) : 1.0f;
+      const uint8_t* srow = XS + (size_t)(SC_SMEM ? r : prow[r]) * sstride;
+      for (int g0 = tid; g0 < gall; g0 += BATCH * NT) {
+        uint32_t sv[BATCH];
+#pragma unroll
+        for (int q = 0; q < BATCH; ++q) {
+          const int g = g0 + q * NT;
+          sv[q] = 127u;
+          if (g < G) sv[q] = SC_SMEM ? srow[g] : __ldcg(srow + g);
+        }
+#pragma unroll
+        for (int q = 0; q < BATCH; ++q) {
+          const int g = g0 + q * NT;
+          if (g >= gall) break;
+          xm_s[r * gall + g] = g < G ? e8m0_to_f32(sv[q]) : 1.0f;
+        }
+      }
     }
   } else {
     // bf16: a half-warp converts one 32-group (two values a lane) with a power-of-two shift
@@ -167,61 +210,77 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, const uint8_t* __rest
     // value has exponent in [e_max - 32, e_max], e_max <= 119 and e_min >= -141 (products and
     // partial sums then stay in fp32's normal range, or on its subnormal grid, on both sides).
     // Otherwise the multiplier is 0 and the exact fallback runs for that group.
-    const uint16_t* X = reinterpret_cast<const uint16_t*>(X8);
     const int wp = tid >> 5, half = (tid >> 4) & 1, lane16 = tid & 15;
     const int gall = GB * 8;
     const int total = real * gall;
-    for (int i0 = 2 * wp; i0 < total; i0 += 2 * NCW) {  // uniform trip count per warp
-      const int i = i0 + half;
-      const bool act = i < total;
-      int r = 0, g = 0;
-      uint32_t two = 0;
-      if (act) {
-        r = i / gall;
-        g = i - r * gall;
-        if (g < G) two = __ldcg(reinterpret_cast<const unsigned int*>(X + (size_t)prow[r] * K + 32 * g + 2 * lane16));
-      }
-      int emax = -1000, emin = 1000;
+    const int step = NT / 16;
+    for (int ib = 2 * wp; ib < total; ib += BATCH * step) {  // uniform trip count per warp
+      uint32_t tw[BATCH];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const uint32_t b = (two >> (16 * hh)) & 0xFFFFu;
-        const uint32_t ef = (b >> 7) & 0xFFu, m = b & 0x7Fu;
-        if (ef == 255u || (ef == 0u && m == 0u)) continue;  // NaN/Inf or zero
-        const int e = ef ? (int)ef - 127 : (31 - __clz((int)m)) - 133;
-        emax = max(emax, e);
-        emin = min(emin, e);
-      }
-#pragma unroll
-      for (int o = 8; o >= 1; o >>= 1) {
-        emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-        emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
-      }
-      if (!act) continue;
-      int sigma = 0;
-      bool safe = true;
-      if (emax > -1000) {
-        sigma = 15 - emax;
-        safe = (emax <= 119) && (emin >= -141) && (emax - emin <= 32);
-      }
-      float lo = __uint_as_float(two << 16), hi = __uint_as_float(two & 0xFFFF0000u);
-      if (safe) {
-        const int s1 = min(max(sigma, -126), 127), s2 = sigma - s1;  // 2^sigma as two exact factors
-        const float f1 = __uint_as_float((uint32_t)(127 + s1) << 23);
-        const float f2 = __uint_as_float((uint32_t)(127 + s2) << 23);
-        lo = __fmul_rn(__fmul_rn(lo, f1), f2);
-        hi = __fmul_rn(__fmul_rn(hi, f1), f2);
-      }
-      const __half2 h2 = __floats2half2_rn(lo, hi);
-      const int t = 2 * lane16;
-      *reinterpret_cast<__half2*>(xs_s + xoff(r, g, t >> 3, GB) + ((t & 7) << 1)) = h2;
-      if (lane16 == 0) {
-        float m = 0.0f;  // 0 marks the exact fallback
-        if (g >= G) m = 1.0f;
-        else if (safe) {
-          const int ns = -sigma;  // 2^-sigma, possibly subnormal (exact)
-          m = ns >= -126 ? __uint_as_float((uint32_t)(127 + ns) << 23) : __uint_as_float(0x00400000u >> (-127 - ns));
+      for (int q = 0; q < BATCH; ++q) {
+        const int i = ib + q * step + half;
+        tw[q] = 0u;
+        if (i < total) {
+          const int r = i / gall, g = i - r * gall;
+          if (g < G) {
+            const uint8_t* src = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride + 2 * (32 * g + 2 * lane16);
+            tw[q] = FROM_SMEM ? *reinterpret_cast<const uint32_t*>(src)
+                              : __ldcg(reinterpret_cast<const unsigned int*>(src));
+          }
         }
-        xm_s[r * GB * 8 + g] = m;
+      }
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q) {
+        const int i = ib + q * step + half;
+        const bool act = i < total;
+        const uint32_t two = tw[q];
+        int r = 0, g = 0;
+        if (act) {
+          r = i / gall;
+          g = i - r * gall;
+        }
+        int emax = -1000, emin = 1000;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const uint32_t bb = (two >> (16 * hh)) & 0xFFFFu;
+          const uint32_t ef = (bb >> 7) & 0xFFu, m = bb & 0x7Fu;
+          if (ef == 255u || (ef == 0u && m == 0u)) continue;  // NaN/Inf or zero
+          const int e = ef ? (int)ef - 127 : (31 - __clz((int)m)) - 133;
+          emax = max(emax, e);
+          emin = min(emin, e);
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+          emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+          emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
+        }
+        if (!act) continue;
+        int sigma = 0;
+        bool safe = true;
+        if (emax > -1000) {
+          sigma = 15 - emax;
+          safe = (emax <= 119) && (emin >= -141) && (emax - emin <= 32);
+        }
+        float lo = __uint_as_float(two << 16), hi = __uint_as_float(two & 0xFFFF0000u);
+        if (safe) {
+          const int s1 = min(max(sigma, -126), 127), s2 = sigma - s1;  // 2^sigma as two exact factors
+          const float f1 = __uint_as_float((uint32_t)(127 + s1) << 23);
+          const float f2 = __uint_as_float((uint32_t)(127 + s2) << 23);
+          lo = __fmul_rn(__fmul_rn(lo, f1), f2);
+          hi = __fmul_rn(__fmul_rn(hi, f1), f2);
+        }
+        const __half2 h2 = __floats2half2_rn(lo, hi);
+        const int t = 2 * lane16;
+        *reinterpret_cast<__half2*>(xs_s + xoff(r, g, t >> 3, GB) + ((t & 7) << 1)) = h2;
+        if (lane16 == 0) {
+          float m = 0.0f;  // 0 marks the exact fallback
+          if (g >= G) m = 1.0f;
+          else if (safe) {
+            const int ns = -sigma;  // 2^-sigma, possibly subnormal (exact)
+            m = ns >= -126 ? __uint_as_float((uint32_t)(127 + ns) << 23) : __uint_as_float(0x00400000u >> (-127 - ns));
+          }
+          xm_s[r * gall + g] = m;
+        }
       }
     }
   }
@@ -229,7 +288,7 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, const uint8_t* __rest
 
 // Row lists of a small launch, computed in shared memory (fused layer): per-pair expert (or -1
 // if left out), per-expert counts -> offsets, active experts, stable positions, per-row slot
-// counts. All NTHREADS threads take part. Ints used: 3E + 2 + 3P + R.
+// counts. All NTHREADS threads take part. Ints used: 3E + 2 + 3P + R + 2 * (NTHREADS / 32).
 struct SRoute {
   int *offs, *prow, *pslot, *act, *rowcnt, *ev, *cnt, *nact;
 };
@@ -245,15 +304,16 @@ __device__ void route_smem(const RowsParams& p, int* base, SRoute& rt, int tid) 
   rt.rowcnt = rt.pslot + P;     // R
   for (int i = tid; i < E; i += NTHREADS) rt.cnt[i] = 0;
   for (int i = tid; i < p.R; i += NTHREADS) rt.rowcnt[i] = 0;
+  for (int q = tid; q < P; q += NTHREADS) rt.prow[q] = p.ids[q];  // ids, staged (prow is free until the scatter)
   __syncthreads();
   int bad = 0;
   for (int q = tid; q < P; q += NTHREADS) {
-    const int e = p.ids[q];
+    const int e = rt.prow[q];
     int v = e;
     if (e < 0 || e >= E) { v = -1; bad |= TFX_ST_RANGE; }
     else {
       for (int jj = q - q % k; jj < q; ++jj)
-        if (p.ids[jj] == e) { v = -1; bad |= TFX_ST_DUP; break; }
+        if (rt.prow[jj] == e) { v = -1; bad |= TFX_ST_DUP; break; }
     }
     rt.ev[q] = v;
     if (v >= 0) {
@@ -263,77 +323,133 @@ __device__ void route_smem(const RowsParams& p, int* base, SRoute& rt, int tid) 
   }
   if (bad && blockIdx.x == 0) report(p.status, bad);
   __syncthreads();
-  if (tid < 32) {  // one warp: exclusive scan of counts and the active list
-    int base_off = 0, base_act = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      const int e = e0 + tid;
-      const int c = e < E ? rt.cnt[e] : 0;
-      int inc = c, a = c > 0 ? 1 : 0;
+  // Exclusive scan of the counts and of the active flags over the whole block: every thread
+  // takes a contiguous run of experts, the warps scan the run totals, warp 0 scans the warp
+  // totals.
+  constexpr int NW = NTHREADS / 32;
+  int* wsum = rt.rowcnt + p.R;  // 2 * NW
+  const int lane = tid & 31, warp = tid >> 5;
+  const int per = (E + NTHREADS - 1) / NTHREADS;
+  const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+  int c_run = 0, a_run = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = rt.cnt[e];
+    c_run += c;
+    a_run += c > 0;
+  }
+  int ci = c_run, ai = a_run;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, o), w = __shfl_up_sync(0xffffffffu, a, o);
-        if (tid >= o) { inc += v; a += w; }
-      }
-      if (e < E) {
-        rt.offs[e] = base_off + inc - c;
-        if (c > 0) rt.act[base_act + a - 1] = e;
-      }
-      base_off += __shfl_sync(0xffffffffu, inc, 31);
-      base_act += __shfl_sync(0xffffffffu, a, 31);
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, ci, o), w = __shfl_up_sync(0xffffffffu, ai, o);
+    if (lane >= o) { ci += v; ai += w; }
+  }
+  if (lane == 31) {
+    wsum[warp] = ci;
+    wsum[NW + warp] = ai;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int c = lane < NW ? wsum[lane] : 0, a = lane < NW ? wsum[NW + lane] : 0;
+    int cs = c, as = a;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, cs, o), w = __shfl_up_sync(0xffffffffu, as, o);
+      if (lane >= o) { cs += v; as += w; }
     }
-    if (tid == 0) {
-      rt.offs[E] = base_off;
-      *rt.nact = base_act;
+    __syncwarp();
+    if (lane < NW) {
+      wsum[lane] = cs - c;
+      wsum[NW + lane] = as - a;
+    }
+    if (lane == 31) {
+      rt.offs[E] = cs;
+      *rt.nact = as;
     }
   }
   __syncthreads();
-  for (int q = tid; q < P; q += NTHREADS) {
-    const int e = rt.ev[q];
-    if (e < 0) continue;
-    int rank = 0;
-    for (int qq = 0; qq < q; ++qq) rank += rt.ev[qq] == e;
-    const int pos = rt.offs[e] + rank;
-    rt.prow[pos] = q / k;
-    rt.pslot[pos] = q % k;
+  {
+    int off = wsum[warp] + ci - c_run, na = wsum[NW + warp] + ai - a_run;
+    for (int e = e0; e < e1; ++e) {
+      const int c = rt.cnt[e];
+      rt.offs[e] = off;
+      rt.cnt[e] = off;  // from here on: the expert's next free position
+      off += c;
+      if (c > 0) rt.act[na++] = e;
+    }
+  }
+  __syncthreads();
+  // Stable scatter, one warp, 32 pairs at a time: a pair's position is its expert's cursor plus
+  // the number of earlier lanes of the chunk with the same expert.
+  if (warp == 0) {
+    for (int q0 = 0; q0 < P; q0 += 32) {
+      const int q = q0 + lane;
+      const int e = q < P ? rt.ev[q] : -2;
+      const unsigned m = __match_any_sync(0xffffffffu, e);
+      if (e >= 0) {
+        const int pos = rt.cnt[e] + __popc(m & ((1u << lane) - 1u));
+        rt.prow[pos] = q / k;
+        rt.pslot[pos] = q - (q / k) * k;
+      }
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(m) - 1) rt.cnt[e] += __popc(m);
+      __syncwarp();
+    }
   }
   __syncthreads();
 }
 
 // ---------------------------------------------------------------- one pass of T rows
-// Consumes the pass's S stages from the ring and leaves the eight-way-tree results of both
-// columns of every real row in epi[r][0..63] (column o at o, column 32 + o at 32 + o).
+// Barriers of the shared-memory handoffs between the roles.
+struct Bars {
+  uint64_t *full, *empty;   // weight ring: producer -> consumers, consumers -> producer
+  uint64_t *xfull, *xempty; // activation buffers: helper -> consumers, consumers -> helper
+  uint64_t *efull, *eempty; // result buffers: consumers -> helper, helper -> consumers
+};
+
+// Bounded wait whose outcome is uniform across the calling warp; on failure the block is
+// marked aborted (the caller then skips its remaining work and waits).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const RowsParams& P,
+                                          volatile int* abort_flag, bool& dead) {
+  if (dead) return false;
+  bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, P.timeout_ns);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) {
+    dead = true;
+    if ((threadIdx.x & 31) == 0) {
+      if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+  return ok;
+}
+
+// Consumers: consume the pass's S weight stages against activation buffer xs_s/xm_s, release
+// the buffer, then hand the eight-way-tree results of both columns of every real row to the
+// helper in epi[r][0..63] (column o at o, column 32 + o at 32 + o).
 template <int KIND, int T>
-__device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, uint8_t* ring, uint64_t* full,
-                                         uint64_t* empty, volatile int* abort_flag, const uint8_t* xs_s,
-                                         const float* xm_s, const int* prow, const uint16_t* xraw, int real,
-                                         uint32_t& it, bool& dead, float* epi) {
+__device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, uint8_t* ring, const Bars& B,
+                                         int bx, int be, uint32_t eph, bool ewait, volatile int* abort_flag,
+                                         const uint8_t* xs_s, const float* xm_s, const int* prow,
+                                         const uint16_t* xraw, int real, uint32_t& it, bool& dead, float* epi) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = lane & 7, o = (warp << 2) | (lane >> 3);
   const int NST = P.nstage, GB = pj.GB;
   float acc0[T], acc1[T];
   int xr[T];
+  const uint8_t* xrow_s[T];
+  const float* xmrow_s[T];
 #pragma unroll
   for (int r = 0; r < T; ++r) {
     acc0[r] = 0.0f;
     acc1[r] = 0.0f;
     xr[r] = min(r, real - 1);
+    xrow_s[r] = xs_s + xr[r] * GB * 512 + j * 16;
+    xmrow_s[r] = xm_s + xr[r] * GB * 8 + j;
   }
   for (int s = 0; s < pj.S; ++s, ++it) {
     const int slot = it % NST;
     const uint32_t ph = (it / NST) & 1u;
-    if (!dead) {
-      // warp-uniform outcome, so the full-warp shuffles and reductions after it stay legal
-      bool ok = (*abort_flag == 0) && mbar_wait(&full[slot], ph, P.timeout_ns);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        dead = true;
-        if (lane == 0) {
-          report(P.status, TFX_ST_TIMEOUT);
-          *abort_flag = 1;
-        }
-      }
-    }
-    if (!dead) {
+    if (warp_wait(&B.full[slot], ph, P, abort_flag, dead)) {
       const uint8_t* tile = ring + (size_t)slot * STAGE_B;
       const uint8_t* sc = tile + TROWS * CODE_B;
       const uint4 cA0 = *reinterpret_cast<const uint4*>(tile + o * CODE_B + 16 * j);
@@ -359,8 +475,10 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
         e2m1x8_to_f16x2(wB1[tc], b1[0], b1[1], b1[2], b1[3]);
 #pragma unroll
         for (int r = 0; r < T; ++r) {
-          const uint4 xa = *reinterpret_cast<const uint4*>(xs_s + xoff(xr[r], gA, tc, GB));
-          const uint4 xb = *reinterpret_cast<const uint4*>(xs_s + xoff(xr[r], gB, tc, GB));
+          // xoff(row, 16s + j (+ 8), tc) = row*GB*512 + s*1024 (+ 512) + tc*128 + j*16
+          const uint8_t* xp = xrow_s[r] + s * 1024 + tc * 128;
+          const uint4 xa = *reinterpret_cast<const uint4*>(xp);
+          const uint4 xb = *reinterpret_cast<const uint4*>(xp + 512);
           const uint32_t* va = reinterpret_cast<const uint32_t*>(&xa);
           const uint32_t* vb = reinterpret_cast<const uint32_t*>(&xb);
 #pragma unroll
@@ -374,7 +492,7 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
       }
 #pragma unroll
       for (int r = 0; r < T; ++r) {
-        const float mA = xm_s[xr[r] * GB * 8 + gA], mB = xm_s[xr[r] * GB * 8 + gB];
+        const float mA = xmrow_s[r][s * GPS], mB = xmrow_s[r][s * GPS + 8];
         if (KIND == TFX_ACT_E4M3) {
           acc0[r] = __fmaf_rn(pA0[r], __fmul_rn(sA0, mA), acc0[r]);
           acc1[r] = __fmaf_rn(pA1[r], __fmul_rn(sA1, mA), acc1[r]);
@@ -405,9 +523,12 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    if (lane == 0) mbar_arrive(&B.empty[slot]);
   }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&B.xempty[bx]);  // this warp is done with the activation buffer
   // eight-way tree: ((a0+a4)+(a2+a6)) + ((a1+a5)+(a3+a7)) across the octet
+  float v0r[T], v1r[T];
 #pragma unroll
   for (int r = 0; r < T; ++r) {
     float v0 = acc0[r], v1 = acc1[r];
@@ -417,19 +538,30 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
     v1 = v1 + __shfl_xor_sync(0xffffffffu, v1, 2);
     v0 = v0 + __shfl_xor_sync(0xffffffffu, v0, 1);
     v1 = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
-    if (j == 0 && r < real) {
-      epi[r * 64 + o] = v0;
-      epi[r * 64 + 32 + o] = v1;
-    }
+    v0r[r] = v0;
+    v1r[r] = v1;
   }
+  if (ewait) warp_wait(&B.eempty[be], eph, P, abort_flag, dead);
+  if (!dead && j == 0) {
+#pragma unroll
+    for (int r = 0; r < T; ++r)
+      if (r < real) {
+        epi[r * 64 + o] = v0r[r];
+        epi[r * 64 + 32 + o] = v1r[r];
+      }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&B.efull[be]);
 }
 
 template <int KIND, int MAXR, bool DOWN>
 __device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const Proj& pj, uint8_t* ring,
-                                              uint64_t* full, uint64_t* empty, volatile int* abort_flag,
-                                              const uint8_t* xs_s, const float* xm_s, const int* prow,
-                                              const uint16_t* xraw, int real, uint32_t& it, bool& dead, float* epi) {
-#define TFX_PASS(TT) run_pass<KIND, TT>(P, pj, ring, full, empty, abort_flag, xs_s, xm_s, prow, xraw, real, it, dead, epi)
+                                              const Bars& B, int bx, int be, uint32_t eph, bool ewait,
+                                              volatile int* abort_flag, const uint8_t* xs_s, const float* xm_s,
+                                              const int* prow, const uint16_t* xraw, int real, uint32_t& it,
+                                              bool& dead, float* epi) {
+#define TFX_PASS(TT) \
+  run_pass<KIND, TT>(P, pj, ring, B, bx, be, eph, ewait, abort_flag, xs_s, xm_s, prow, xraw, real, it, dead, epi)
   switch (t) {
     case 1: TFX_PASS(1); break;
     case 2: if constexpr (MAXR >= 2) TFX_PASS(2); break;
@@ -441,29 +573,207 @@ __device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const 
 #undef TFX_PASS
 }
 
+// One pass as the helper sees it (all fields warp-uniform).
+struct HPass {
+  bool dn, last;
+  int a, u, real, pidx;
+  int pair[8];
+};
+
+// Helper: the epilogue of one pass, from result buffer epi. Gate/up: SwiGLU, the activation
+// quantiser and h (+ debug copies); fused launches publish a finished gate/up item. Down: the
+// expert outputs d; fused launches combine each (row, block) whose last slot this writes.
+template <int KIND, int PH>
+__device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars& B, const float* epi,
+                                const int* r_prow, const int* r_pslot, const int* r_rowcnt, int32_t* done_upc,
+                                int32_t* slots_done, volatile int* abort_flag, bool& dead) {
+  const int lane = threadIdx.x & 31;
+  const int be = q.pidx & 1;
+  warp_wait(&B.efull[be], (q.pidx >> 1) & 1, P, abort_flag, dead);
+  if (!dead) {
+    for (int r = 0; r < q.real; ++r) {
+      const int p = q.pair[r];
+      if (!q.dn) {
+        const int I = P.I;
+        const int nn = 32 * q.u + lane;
+        const float g = epi[r * 64 + lane], uu = epi[r * 64 + 32 + lane];
+        const float den = __fadd_rn(1.0f, expf(-g));
+        const float hv = __fmul_rn(__fdiv_rn(g, den), uu);
+        if (P.gu_dbg) {
+          P.gu_dbg[(size_t)p * 2 * I + nn] = g;
+          P.gu_dbg[(size_t)p * 2 * I + I + nn] = uu;
+        }
+        if (P.h_dbg) P.h_dbg[(size_t)p * I + nn] = hv;
+        if (KIND == TFX_ACT_E4M3) {
+          const bool bad = __any_sync(0xffffffffu, isnan(hv) || isinf(hv));
+          const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+          uint32_t sc;
+          if (bad) sc = 255u;
+          else if (amax_b == 0u) sc = 127u;
+          else {
+            const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
+            sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
+          }
+          const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv, e8m0_recip_f32(sc)));
+          static_cast<uint8_t*>(P.h)[(size_t)p * I + nn] = (uint8_t)code;
+          if (lane == 0) P.hs[(size_t)p * (I / 32) + q.u] = (uint8_t)sc;
+        } else {
+          static_cast<__nv_bfloat16*>(P.h)[(size_t)p * I + nn] = __float2bfloat16_rn(hv);
+        }
+      } else {
+        const int row = r_prow[p], slot = r_pslot[p];
+        if (row >= 0 && row < P.R && slot >= 0 && slot < P.k) {
+          float* dst = P.out + ((size_t)row * P.k + slot) * P.H + 64 * q.u;
+          dst[lane] = epi[r * 64 + lane];
+          dst[32 + lane] = epi[r * 64 + 32 + lane];
+          if (PH == PH_FUSED) {
+            // combine (row, block u) in the CTA that writes the row's last slot
+            __threadfence();
+            int last = 0;
+            if (lane == 0) last = atomicAdd(&slots_done[(size_t)row * P.pd.units + q.u], 1) == r_rowcnt[row] - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+              __threadfence();
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int m = 64 * q.u + 32 * hh + lane;
+                float yv = 0.0f;
+                for (int jj = 0; jj < P.k; ++jj)
+                  yv = __fmaf_rn(P.topk_w[(size_t)row * P.k + jj], __ldcg(P.out + ((size_t)row * P.k + jj) * P.H + m), yv);
+                P.y[(size_t)row * P.H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+                if (P.y32) P.y32[(size_t)row * P.H + m] = yv;
+              }
+            }
+          }
+        } else if (lane == 0) {
+          report(P.status, TFX_ST_SHAPE);
+        }
+      }
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&B.eempty[be]);
+  if (PH == PH_FUSED && !q.dn && q.last) {  // publish a finished gate/up item
+    __threadfence();
+    __syncwarp();
+    if (lane == 0 && !dead) atomicAdd(done_upc + q.a, 1);
+  }
+}
+
+// ---------------------------------------------------------------- the sequence of passes
+// Every role walks the same sequence: this CTA's items (blockIdx.x + i * gridDim.x; gate/up
+// items before down items), and within an item its passes sized by the rows left.
+struct PassDesc {
+  bool dn, first, last;
+  int a, u, e, p0, pos, real, t, pidx;
+};
+struct PassGen {
+  int item, left, pos, pidx;
+  bool open, done;
+  bool dn;
+  int a, u, e, p0;
+};
+struct SeqCtx {
+  int total, n_upc;
+  const int *act, *offs;
+};
+// next_item() yields this CTA's next item index, or -1 when there is none.
+template <int MAXR_U, int MAXR_D, typename NextItem>
+__device__ __forceinline__ bool gen_next(PassGen& g, PassDesc& d, const RowsParams& P, const SeqCtx& c,
+                                         NextItem&& next_item) {
+  while (true) {
+    if (!g.open) {
+      if (g.done) return false;
+      g.item = next_item();
+      if (g.item < 0 || g.item >= c.total) {
+        g.done = true;
+        return false;
+      }
+      const bool dn = g.item >= c.n_upc;
+      const Proj& pj = dn ? P.pd : P.pu;
+      const int li = dn ? g.item - c.n_upc : g.item;
+      const int a = li / pj.units, u = li - a * pj.units;
+      const int e = c.act[a];
+      const int p0 = (e >= 0 && e < P.E) ? c.offs[e] : 0;
+      const int n = (e >= 0 && e < P.E) ? c.offs[e + 1] - p0 : 0;
+      if (e < 0 || e >= P.E || n <= 0 || p0 < 0 || p0 + n > P.R * P.k) {
+        if (n != 0 && threadIdx.x == 0) report(P.status, TFX_ST_SHAPE);
+        continue;
+      }
+      g.open = true;
+      g.dn = dn;
+      g.a = a;
+      g.u = u;
+      g.e = e;
+      g.p0 = p0;
+      g.pos = p0;
+      g.left = n;
+    }
+    const int t = g.dn ? tier_of<true>(g.left, MAXR_D, P.tier_mode) : tier_of<false>(g.left, MAXR_U, P.tier_mode);
+    const int real = min(t, g.left);
+    d.dn = g.dn;
+    d.first = g.pos == g.p0;
+    d.last = g.left == real;
+    d.a = g.a;
+    d.u = g.u;
+    d.e = g.e;
+    d.p0 = g.p0;
+    d.pos = g.pos;
+    d.real = real;
+    d.t = t;
+    d.pidx = g.pidx++;
+    g.pos += real;
+    g.left -= real;
+    if (g.left == 0) g.open = false;
+    return true;
+  }
+}
+
 // ---------------------------------------------------------------- the kernel
+// Roles: warps 0..7 consume (compute); warp 8 produces (weight stages); warp 9 stages: it
+// brings each pass's activation rows in by bulk copy one pass ahead and converts them into
+// the f16 buffer; warp 10 runs each pass's epilogue (SwiGLU and quantisation of h, or the d
+// rows and, in the fused launch, the combine) while the consumers go on with the next pass.
 template <int KIND, int MAXR_U, int MAXR_D, int PH>
 __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <= 2 ? 2 : 1)
     rows_kernel(const RowsParams P) {
   constexpr int MAXR = ((PH & PH_UPC) && MAXR_U > MAXR_D) || !(PH & PH_DOWN) ? MAXR_U : MAXR_D;
+  constexpr int AB = KIND == TFX_ACT_E4M3 ? 1 : 2;  // activation bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
   const Layout Ly = layout_of(P, MAXR);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Ly.bars);
-  uint64_t* empty = full + MAX_NSTAGE;
+  Bars B;
+  B.full = reinterpret_cast<uint64_t*>(smem + Ly.bars);
+  B.empty = B.full + MAX_NSTAGE;
+  B.xfull = B.empty + MAX_NSTAGE;
+  B.xempty = B.xfull + 2;
+  B.efull = B.xempty + 2;
+  B.eempty = B.efull + 2;
+  uint64_t* rawfull = B.eempty + 2;
+  uint64_t* qfull = rawfull + 1;  // fused: claimed-item queue, producer -> helper and consumers
+  uint64_t* qempty = qfull + QD;  //        and back
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.ctrl);
-  int* prow = reinterpret_cast<int*>(smem + Ly.pass);
-  int* ppair = prow + 8;
-  float* epi = reinterpret_cast<float*>(smem + Ly.epi);
+  int* pdesc = reinterpret_cast<int*>(smem + Ly.pdesc);  // [2][16]: prow[8], ppair[8]
+  float* epi = reinterpret_cast<float*>(smem + Ly.epi);    // [2][8][64]
   uint8_t* ring = smem + Ly.ring;
-  uint8_t* xs_s = smem + Ly.xs;
-  float* xm_s = reinterpret_cast<float*>(smem + Ly.xm);
+  uint8_t* raw = smem + Ly.raw;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NST = P.nstage;
+  const int NST = P.nstage, NXB = P.nxb;
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], NCW);
+      mbar_init(&B.full[s], 1);
+      mbar_init(&B.empty[s], NCW);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&B.xfull[b], 1);
+      mbar_init(&B.xempty[b], NCW);
+      mbar_init(&B.efull[b], NCW);
+      mbar_init(&B.eempty[b], 1);
+    }
+    mbar_init(rawfull, 1);
+    for (int b = 0; b < QD; ++b) {
+      mbar_init(&qfull[b], 1);
+      mbar_init(&qempty[b], NCW + 2);
     }
     mbar_fence_init();
     *abort_flag = 0;
@@ -499,182 +809,284 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
     r_pslot = P.pair_slot;
     r_act = P.active;
   }
-  const int n_upc = (PH & PH_UPC) ? n_act * P.pu.units : 0;
-  const int n_down = (PH & PH_DOWN) ? n_act * P.pd.units : 0;
-  const int total = n_upc + n_down;
-  int32_t* done_upc = PH == PH_FUSED ? P.scratch + 1 : nullptr;
-  int32_t* slots_done = PH == PH_FUSED ? P.scratch + 1 + P.E : nullptr;
+  SeqCtx sc;
+  sc.n_upc = (PH & PH_UPC) ? n_act * P.pu.units : 0;
+  sc.total = sc.n_upc + ((PH & PH_DOWN) ? n_act * P.pd.units : 0);
+  sc.act = r_act;
+  sc.offs = r_offs;
+  int32_t* work_ctr = PH == PH_FUSED ? P.scratch + 1 : nullptr;
+  int32_t* done_upc = PH == PH_FUSED ? P.scratch + 2 : nullptr;
+  int32_t* slots_done = PH == PH_FUSED ? P.scratch + 2 + P.E : nullptr;
+  int* qid = reinterpret_cast<int*>(smem + Ly.ctrl + 16);  // [QD] claimed item ids
+  PassGen gen = {};
+  PassDesc d;
+  // Separate launches stride over the items; the fused launch hands items out dynamically: the
+  // producer claims them from a global counter, in order (gate/up items expert by expert, then
+  // down items), and passes them to the helper and the consumers through a small queue.
+  int static_next = blockIdx.x - (int)gridDim.x;
+  uint32_t qpos = 0;
+  auto next_static = [&]() { static_next += gridDim.x; return static_next; };
+  auto next_popped = [&]() {  // helper and consumers (warp-wide)
+    const int slot = qpos % QD;
+    bool dq = false;
+    warp_wait(&qfull[slot], (qpos / QD) & 1, P, abort_flag, dq);
+    int v = dq ? -1 : qid[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(&qempty[slot]);
+    ++qpos;
+    return v;
+  };
 
-  if (warp == NCW) {
+  if (warp == W_PROD) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t it = 0;
       bool stop = false;
-      for (int item = blockIdx.x; item < total && !stop; item += gridDim.x) {
-        const bool dn = item >= n_upc;
-        const Proj& pj = dn ? P.pd : P.pu;
-        const int li = dn ? item - n_upc : item;
-        const int a = li / pj.units, u = li - a * pj.units;
-        const int e = r_act[a];
-        if (e < 0 || e >= P.E) continue;
-        const int p0 = r_offs[e], n = r_offs[e + 1] - p0;
-        if (n <= 0 || p0 < 0 || p0 + n > P.R * P.k) continue;
-        const uint8_t* src = pj.w + (size_t)e * pj.expert_bytes + (size_t)u * pj.unit_bytes;
-        for (int left = n; left > 0 && !stop;) {
-          const int t = dn ? tier_of<true>(left, MAXR_D, P.tier_mode) : tier_of<false>(left, MAXR_U, P.tier_mode);
-          left -= min(t, left);
-          for (int s = 0; s < pj.S; ++s, ++it) {
-            const int slot = it % NST;
-            const uint32_t ph = (it / NST) & 1u;
-            if (*abort_flag) { stop = true; break; }
-            if (it >= (uint32_t)NST && !mbar_wait(&empty[slot], ph ^ 1u, P.timeout_ns)) {
-              report(P.status, TFX_ST_TIMEOUT);
-              *abort_flag = 1;
-              stop = true;
-              break;
-            }
-            if (*abort_flag) { stop = true; break; }
-            mbar_arrive_expect_tx(&full[slot], STAGE_B);
-            bulk_g2s(ring + (size_t)slot * STAGE_B, src + (size_t)s * STAGE_B, STAGE_B, &full[slot]);
+      uint32_t claims = 0;
+      auto claim = [&]() {  // producer lane: claim an item and publish it to the queue
+        const int slot = claims % QD;
+        int v = -1;
+        if (claims >= (uint32_t)QD && !mbar_wait(&qempty[slot], ((claims / QD) & 1) ^ 1, P.timeout_ns)) {
+          if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
+          *abort_flag = 1;
+        } else if (!*abort_flag) {
+          // a CTA's first item is its own index; the counter hands out the rest
+          v = claims == 0 ? (int)blockIdx.x : atomicAdd(work_ctr, 1) + (int)gridDim.x;
+          if (v >= sc.total) v = -1;
+        }
+        qid[slot] = v;
+        mbar_arrive(&qfull[slot]);
+        ++claims;
+        return v;
+      };
+      // The queue runs one item ahead of the producer, so the stager learns of the next item
+      // (and can stage its activations) while the current one streams. The claim of that next
+      // item is made once the current item's first stages are on their way.
+      int ahead = -2;
+      bool pending = false;
+      auto claim_pending = [&]() {
+        if (pending) {
+          ahead = claim();
+          pending = false;
+        }
+      };
+      auto next_claimed = [&]() {
+        if (ahead == -2) ahead = claim();
+        claim_pending();
+        const int v = ahead;
+        if (v >= 0) pending = true;
+        else ahead = -1;
+        return v;
+      };
+      auto next_prod = [&]() { return PH == PH_FUSED ? next_claimed() : next_static(); };
+      while (!stop && gen_next<MAXR_U, MAXR_D>(gen, d, P, sc, next_prod)) {
+        const Proj& pj = d.dn ? P.pd : P.pu;
+        const uint8_t* src = pj.w + (size_t)d.e * pj.expert_bytes + (size_t)d.u * pj.unit_bytes;
+        for (int s = 0; s < pj.S; ++s, ++it) {
+          const int slot = it % NST;
+          const uint32_t ph = (it / NST) & 1u;
+          if (*abort_flag) { stop = true; break; }
+          if (it >= (uint32_t)NST && !mbar_wait(&B.empty[slot], ph ^ 1u, P.timeout_ns)) {
+            if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
+            *abort_flag = 1;
+            stop = true;
+            break;
           }
+          if (*abort_flag) { stop = true; break; }
+          mbar_arrive_expect_tx(&B.full[slot], STAGE_B);
+          bulk_g2s(ring + (size_t)slot * STAGE_B, src + (size_t)s * STAGE_B, STAGE_B, &B.full[slot]);
+          if (PH == PH_FUSED && (it + 1 >= (uint32_t)NST || s == pj.S - 1)) claim_pending();
+        }
+      }
+      if (PH == PH_FUSED) claim_pending();
+      if (PH == PH_FUSED && !gen.done) {
+        // stopped early (abort): tell the helper and the consumers there is nothing more
+        *abort_flag = 1;
+        for (int q = 0; q < 2 * QD && !gen.done; ++q) {
+          const int slot = claims % QD;
+          mbar_wait(&qempty[slot], ((claims / QD) & 1) ^ 1, 1000000ull);
+          qid[slot] = -1;
+          mbar_arrive(&qfull[slot]);
+          ++claims;
         }
       }
       // Drain: every issued stage must have landed before the block may exit.
       const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
       for (uint32_t q = first; q < it; ++q) {
-        if (!mbar_wait(&full[q % NST], (q / NST) & 1u, P.timeout_ns)) {
+        if (!mbar_wait(&B.full[q % NST], (q / NST) & 1u, P.timeout_ns)) {
           report(P.status, TFX_ST_TIMEOUT);
           break;
         }
       }
     }
+  } else if (warp == W_HELP) {
+    // ---------------------------------------------------------------- helper
+    bool dead = false;
+    uint32_t raw_issued = 0, raw_waited = 0;
+
+    // rows of a pass: token rows (gate/up) or pair rows (down); padding repeats the last
+    auto row_of = [&](const PassDesc& q, int r) {
+      const int src = q.pos + min(r, q.real - 1);
+      if (q.dn) return src;
+      const int row = r_prow[src];
+      return (row < 0 || row >= P.R) ? 0 : row;
+    };
+    // fused down: wait (bounded) until every gate/up item of the expert has published its h
+    auto wait_dependency = [&](const PassDesc& q) {
+      if (!(PH == PH_FUSED && q.dn && q.first) || dead) return;
+      int okw = 1;
+      if (lane == 0) {
+        const uint64_t t0 = global_ns();
+        while (true) {
+          int v;
+          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(done_upc + q.a) : "memory");
+          if (v >= P.pu.units) break;
+          if (*abort_flag || global_ns() - t0 > P.timeout_ns) {
+            if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
+            *abort_flag = 1;
+            okw = 0;
+            break;
+          }
+          __nanosleep(64);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read next by the async proxy
+      }
+      if (!__shfl_sync(0xffffffffu, okw, 0)) dead = true;
+    };
+    // bulk copies of the pass's activation rows (and scales) into the raw buffer
+    // Rows of the pass last staged into each activation buffer (lane r < 8 holds row r): a pass
+    // whose buffer already holds its rows (every gate/up pass of a one-row launch, for one) is
+    // not staged again.
+    int krow0 = -1, krow1 = -1, kdn0 = -1, kdn1 = -1, kreal0 = 0, kreal1 = 0;
+    bool pend_skip = false;
+    auto same_rows = [&](const PassDesc& q) {
+      const bool b1 = NXB == 2 && (q.pidx & 1);
+      const int mine = lane < 8 ? row_of(q, lane) : 0;
+      const bool eq = lane >= 8 || (b1 ? krow1 : krow0) == mine;
+      return (b1 ? kdn1 : kdn0) == (int)q.dn && (b1 ? kreal1 : kreal0) == q.real && __all_sync(0xffffffffu, eq);
+    };
+    auto issue_raw = [&](const PassDesc& q) {
+      pend_skip = same_rows(q);
+      if (pend_skip || !P.use_raw || dead) return;
+      const Proj& pj = q.dn ? P.pd : P.pu;
+      const int rowb = pj.K * AB;
+      const bool tsc = KIND == TFX_ACT_E4M3 && (q.dn ? P.sc_tma_d : P.sc_tma_u);
+      const uint8_t* X8 = q.dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
+      const uint8_t* XS = q.dn ? P.hs : P.xs;
+      int rows[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) rows[r] = row_of(q, r);
+      __syncwarp();  // the previous conversion's reads of the raw buffer are done
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(rawfull, (uint32_t)(q.real * (rowb + (tsc ? pj.G : 0))));
+        for (int r = 0; r < q.real; ++r) {
+          bulk_g2s(raw + r * P.raw_row, X8 + (size_t)rows[r] * rowb, rowb, rawfull);
+          if (tsc) bulk_g2s(raw + MAXR * P.raw_row + r * P.raw_sc, XS + (size_t)rows[r] * pj.G, pj.G, rawfull);
+        }
+      }
+      ++raw_issued;
+    };
+    // wait for the pass's activation buffer, fill it, hand it to the consumers
+    auto finish_stage = [&](const PassDesc& q) {
+      const Proj& pj = q.dn ? P.pd : P.pu;
+      const int bx = NXB == 2 ? (q.pidx & 1) : 0;
+      if (q.pidx >= NXB) warp_wait(&B.xempty[bx], ((q.pidx / NXB) & 1) ^ 1, P, abort_flag, dead);
+      int* pd = pdesc + 16 * bx;
+      if (lane < 8) {
+        pd[lane] = row_of(q, lane);
+        pd[8 + lane] = q.pos + min(lane, q.real - 1);
+      }
+      __syncwarp();
+      uint8_t* xs_s = smem + Ly.xs + bx * Ly.xs_stride;
+      float* xm_s = reinterpret_cast<float*>(smem + Ly.xm + bx * Ly.xm_stride);
+      const uint8_t* X8 = q.dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
+      const uint8_t* XS = q.dn ? P.hs : P.xs;
+      if (pend_skip) {
+        // the buffer holds these rows already
+      } else if (P.use_raw) {
+        if (raw_waited < raw_issued) {
+          warp_wait(rawfull, raw_waited & 1u, P, abort_flag, dead);
+          ++raw_waited;
+        }
+        const bool tsc = KIND == TFX_ACT_E4M3 && (q.dn ? P.sc_tma_d : P.sc_tma_u);
+        if (!dead) {
+          if (tsc)
+            stage_rows<KIND, true, true>(raw, P.raw_row, raw + MAXR * P.raw_row, P.raw_sc, pj.K, pj.G, pj.GB, xs_s,
+                                         xm_s, pd, q.real, lane, 32);
+          else
+            stage_rows<KIND, true, false>(raw, P.raw_row, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
+                                          lane, 32);
+        }
+      } else if (!dead) {
+        stage_rows<KIND, false, false>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
+                                       lane, 32);
+      }
+      if (!pend_skip && !dead) {
+        const int mine = lane < 8 ? row_of(q, lane) : 0;
+        if (bx) { krow1 = mine; kdn1 = q.dn; kreal1 = q.real; }
+        else { krow0 = mine; kdn0 = q.dn; kreal0 = q.real; }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&B.xfull[bx]);
+    };
+    PassDesc cur, nxt;
+    auto next_hc = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
+    bool hc = gen_next<MAXR_U, MAXR_D>(gen, cur, P, sc, next_hc);
+    if (hc) {
+      wait_dependency(cur);
+      issue_raw(cur);
+    }
+    while (hc) {
+      finish_stage(cur);
+      if (!gen_next<MAXR_U, MAXR_D>(gen, nxt, P, sc, next_hc)) break;
+      wait_dependency(nxt);
+      issue_raw(nxt);
+      cur = nxt;
+    }
+    // a bulk copy issued before an abort must land before the block may exit
+    if (lane == 0 && raw_waited < raw_issued && !mbar_wait(rawfull, raw_waited & 1u, P.timeout_ns))
+      report(P.status, TFX_ST_TIMEOUT);
+  } else if (warp == W_EPI) {
+    // ---------------------------------------------------------------- epilogue
+    bool dead = false;
+    auto epilogue = [&](const PassDesc& q) {
+      HPass hp;
+      hp.dn = q.dn;
+      hp.last = q.last;
+      hp.a = q.a;
+      hp.u = q.u;
+      hp.real = q.real;
+      hp.pidx = q.pidx;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) hp.pair[r] = q.pos + min(r, q.real - 1);
+      helper_epilogue<KIND, PH>(P, hp, B, epi + (q.pidx & 1) * 512, r_prow, r_pslot, r_rowcnt, done_upc, slots_done,
+                                abort_flag, dead);
+    };
+
+    auto next_e = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
+    PassDesc q;
+    while (gen_next<MAXR_U, MAXR_D>(gen, q, P, sc, next_e)) epilogue(q);
   } else {
     // ---------------------------------------------------------------- consumers
     uint32_t it = 0;
     bool dead = false;
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-      const bool dn = item >= n_upc;
-      const Proj& pj = dn ? P.pd : P.pu;
-      const int li = dn ? item - n_upc : item;
-      const int a = li / pj.units, u = li - a * pj.units;
-      const int e = r_act[a];
-      if (e < 0 || e >= P.E) { if (tid == 0) report(P.status, TFX_ST_SHAPE); continue; }
-      const int p0 = r_offs[e], n = r_offs[e + 1] - p0;
-      if (n <= 0 || p0 < 0 || p0 + n > P.R * P.k) { if (tid == 0 && n != 0) report(P.status, TFX_ST_SHAPE); continue; }
-      if (PH == PH_FUSED && dn) {
-        // the expert's h must be complete: wait (bounded) for all of its gate/up items
-        if (tid == 0 && !dead) {
-          const uint64_t t0 = global_ns();
-          while (true) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(done_upc + a) : "memory");
-            if (v >= P.pu.units) break;
-            if (*abort_flag || global_ns() - t0 > P.timeout_ns) {
-              report(P.status, TFX_ST_TIMEOUT);
-              *abort_flag = 1;
-              break;
-            }
-            __nanosleep(64);
-          }
-        }
-        named_sync(1, NCONS);
-        if (*abort_flag) dead = true;
-      }
-      const uint8_t* X8 = dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
-      const uint8_t* XS = dn ? P.hs : P.xs;
-      int pos = p0;
-      for (int left = n; left > 0;) {
-        const int t = dn ? tier_of<true>(left, MAXR_D, P.tier_mode) : tier_of<false>(left, MAXR_U, P.tier_mode);
-        const int real = min(t, left);
-        named_sync(1, NCONS);
-        if (tid < 8) {  // pass rows: real rows, then padding rows that repeat the last real row
-          const int src = pos + min(tid, real - 1);
-          int row = src;
-          if (!dn) {
-            row = r_prow[src];
-            if (row < 0 || row >= P.R) { report(P.status, TFX_ST_SHAPE); row = 0; }
-          }
-          prow[tid] = row;
-          ppair[tid] = src;
-        }
-        named_sync(1, NCONS);
-        stage_rows<KIND>(X8, XS, pj.K, pj.G, pj.GB, xs_s, xm_s, prow, real, tid);
-        named_sync(1, NCONS);
-        if (dn) dispatch_pass<KIND, MAXR_D, true>(t, P, pj, ring, full, empty, abort_flag, xs_s, xm_s, prow,
-                                                  reinterpret_cast<const uint16_t*>(X8), real, it, dead, epi);
-        else dispatch_pass<KIND, MAXR_U, false>(t, P, pj, ring, full, empty, abort_flag, xs_s, xm_s, prow,
-                                                reinterpret_cast<const uint16_t*>(X8), real, it, dead, epi);
-        named_sync(1, NCONS);
-
-        // ------------------------------------------------------------ epilogue
-        if (warp < real && !dead) {
-          const int r = warp;
-          const int p = ppair[r];
-          if (!dn) {
-            const int I = P.I;
-            const int nn = 32 * u + lane;
-            const float g = epi[r * 64 + lane], uu = epi[r * 64 + 32 + lane];
-            const float den = __fadd_rn(1.0f, expf(-g));
-            const float hv = __fmul_rn(__fdiv_rn(g, den), uu);
-            if (P.gu_dbg) {
-              P.gu_dbg[(size_t)p * 2 * I + nn] = g;
-              P.gu_dbg[(size_t)p * 2 * I + I + nn] = uu;
-            }
-            if (P.h_dbg) P.h_dbg[(size_t)p * I + nn] = hv;
-            if (KIND == TFX_ACT_E4M3) {
-              const bool bad = __any_sync(0xffffffffu, isnan(hv) || isinf(hv));
-              const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-              uint32_t sc;
-              if (bad) sc = 255u;
-              else if (amax_b == 0u) sc = 127u;
-              else {
-                const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
-                sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
-              }
-              const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv, e8m0_recip_f32(sc)));
-              static_cast<uint8_t*>(P.h)[(size_t)p * I + nn] = (uint8_t)code;
-              if (lane == 0) P.hs[(size_t)p * (I / 32) + u] = (uint8_t)sc;
-            } else {
-              static_cast<__nv_bfloat16*>(P.h)[(size_t)p * I + nn] = __float2bfloat16_rn(hv);
-            }
-          } else {
-            const int row = r_prow[p], slot = r_pslot[p];
-            if (row >= 0 && row < P.R && slot >= 0 && slot < P.k) {
-              float* dst = P.out + ((size_t)row * P.k + slot) * P.H + 64 * u;
-              dst[lane] = epi[r * 64 + lane];
-              dst[32 + lane] = epi[r * 64 + 32 + lane];
-              if (PH == PH_FUSED) {
-                // combine (row, block u) in the CTA that writes its row's last slot
-                __threadfence();
-                int last = 0;
-                if (lane == 0) last = atomicAdd(&slots_done[(size_t)row * P.pd.units + u], 1) == r_rowcnt[row] - 1;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                  __threadfence();
-#pragma unroll
-                  for (int hh = 0; hh < 2; ++hh) {
-                    const int m = 64 * u + 32 * hh + lane;
-                    float yv = 0.0f;
-                    for (int jj = 0; jj < P.k; ++jj)
-                      yv = __fmaf_rn(P.topk_w[(size_t)row * P.k + jj], __ldcg(P.out + ((size_t)row * P.k + jj) * P.H + m), yv);
-                    P.y[(size_t)row * P.H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
-                    if (P.y32) P.y32[(size_t)row * P.H + m] = yv;
-                  }
-                }
-              }
-            } else if (lane == 0) {
-              report(P.status, TFX_ST_SHAPE);
-            }
-          }
-        }
-        pos += real;
-        left -= real;
-      }
-      if (PH == PH_FUSED && !dn) {  // publish this gate/up item
-        __threadfence();
-        named_sync(1, NCONS);
-        if (tid == 0) atomicAdd(done_upc + a, 1);
-      }
+    auto next_c = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
+    while (gen_next<MAXR_U, MAXR_D>(gen, d, P, sc, next_c)) {
+      const Proj& pj = d.dn ? P.pd : P.pu;
+      const int bx = NXB == 2 ? (d.pidx & 1) : 0;
+      const int be = d.pidx & 1;
+      warp_wait(&B.xfull[bx], (d.pidx / NXB) & 1, P, abort_flag, dead);
+      const uint8_t* xs_s = smem + Ly.xs + bx * Ly.xs_stride;
+      const float* xm_s = reinterpret_cast<const float*>(smem + Ly.xm + bx * Ly.xm_stride);
+      const uint16_t* xraw = reinterpret_cast<const uint16_t*>(d.dn ? P.h : P.x);
+      const int* prow = pdesc + 16 * bx;
+      float* ep = epi + be * 512;
+      const uint32_t eph = ((d.pidx >> 1) & 1) ^ 1;
+      if (d.dn) dispatch_pass<KIND, MAXR_D, true>(d.t, P, pj, ring, B, bx, be, eph, d.pidx >= 2, abort_flag, xs_s,
+                                                  xm_s, prow, xraw, d.real, it, dead, ep);
+      else dispatch_pass<KIND, MAXR_U, false>(d.t, P, pj, ring, B, bx, be, eph, d.pidx >= 2, abort_flag, xs_s,
+                                              xm_s, prow, xraw, d.real, it, dead, ep);
     }
   }
   if (PH == PH_FUSED) {
@@ -685,7 +1097,7 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
       const int prev = atomicAdd(P.scratch, 1);
       if (prev == (int)gridDim.x - 1) {
         __threadfence();
-        for (int i = 1; i <= P.E; ++i) P.scratch[i] = 0;
+        for (int i = 1; i <= P.E + 1; ++i) P.scratch[i] = 0;
         const int nc = P.R * P.pd.units;
         for (int i = 0; i < nc; ++i) slots_done[i] = 0;
         __threadfence();
@@ -717,10 +1129,12 @@ static int dev_sms(int* sms, size_t* optin) {
   return TFX_OK;
 }
 
-// Ring depth and blocks per SM: the depth (2..6 stages) that keeps the most stage bytes in
-// flight per SM, fewer stages breaking ties towards more resident blocks. Chosen once per
-// (device, kernel instance, shared-memory shape) and cached, so steady-state launches (and
-// launches under stream capture) issue only the kernel.
+// Shared-memory shape and blocks per SM. Preference: activation rows by bulk copy with two
+// activation buffers (the next pass stages while this one runs), then two buffers fed by
+// global loads, then one buffer. Within a shape, the ring depth (2..6 stages) that keeps the
+// most stage bytes in flight per SM (counting at most 4 stages a block), ties going to more
+// resident blocks. Chosen once per (device, kernel instance, shape) and cached, so that
+// steady-state launches (and launches under stream capture) issue only the kernel.
 template <int KIND, int MAXR_U, int MAXR_D, int PH>
 static int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
   constexpr int MAXR = ((PH & PH_UPC) && MAXR_U > MAXR_D) || !(PH & PH_DOWN) ? MAXR_U : MAXR_D;
@@ -729,7 +1143,7 @@ static int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
   int rc = dev_sms(&sms, &optin);
   if (rc) return rc;
   auto kern = rows_kernel<KIND, MAXR_U, MAXR_D, PH>;
-  struct Entry { int key_gb, key_route, nst, nb; size_t smem; };
+  struct Entry { int key_gb, key_route, key_raw, nst, nxb, use_raw, nb; size_t smem; };
   static Entry cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TFX_ECUDA;
@@ -737,34 +1151,41 @@ static int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(g_mu);
     ent = cache[dev];
-    if (ent.nb == 0 || ent.key_gb != P.gbmax || ent.key_route != P.route_ints) {
+    if (ent.nb == 0 || ent.key_gb != P.gbmax || ent.key_route != P.route_ints || ent.key_raw != P.raw_row) {
       RowsParams q = P;
       q.nstage = 6;
+      q.nxb = 2;
+      q.use_raw = 1;
       const size_t smax = (size_t)layout_of(q, MAXR).total;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)min(smax, optin)) != cudaSuccess)
         return TFX_ELAUNCH;
-      int best = -1, best_nst = 0, best_nb = 0;
-      size_t best_smem = 0;
-      for (int nst = 2; nst <= 6; ++nst) {
-        q.nstage = nst;
-        const size_t sm = (size_t)layout_of(q, MAXR).total;
-        if (sm > optin) break;
-        int nb = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NTHREADS, sm) != cudaSuccess) return TFX_ELAUNCH;
-        if (nb < 1) break;
-        const int score = nb * nst;
-        if (score > best || (score == best && nb > best_nb)) {
-          best = score;
-          best_nst = nst;
-          best_nb = nb;
-          best_smem = sm;
+      const int shapes[4][2] = {{1, 2}, {0, 2}, {1, 1}, {0, 1}};  // (raw, buffers) in order of preference
+      Entry best = {};
+      int best_score = -1;
+      for (int sh = 0; sh < 4 && best_score < 0; ++sh) {
+        for (int nst = 2; nst <= 6; ++nst) {
+          q.nstage = nst;
+          q.use_raw = shapes[sh][0];
+          q.nxb = shapes[sh][1];
+          const size_t sm = (size_t)layout_of(q, MAXR).total;
+          if (sm > optin) break;
+          int nb = 0;
+          if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NTHREADS, sm) != cudaSuccess) return TFX_ELAUNCH;
+          if (nb < 1) break;
+          const int score = nb * min(nst, 4);
+          if (score > best_score || (score == best_score && nb > best.nb)) {
+            best_score = score;
+            best = Entry{P.gbmax, P.route_ints, P.raw_row, nst, q.nxb, q.use_raw, nb, sm};
+          }
         }
       }
-      if (best_nst == 0) return TFX_EUNSUPPORTED;
-      ent = Entry{P.gbmax, P.route_ints, best_nst, best_nb, best_smem};
+      if (best_score < 0) return TFX_EUNSUPPORTED;
+      ent = best;
       cache[dev] = ent;
     }
   }
+  P.use_raw = ent.use_raw;
+  P.nxb = ent.nxb;
   P.nstage = ent.nst;
   const int grid = min(max_items, ent.nb * sms);
   if (grid < 1) return TFX_OK;
@@ -810,6 +1231,14 @@ static Proj proj_of(const tfx_dims& d, bool down, const uint8_t* w) {
   p.expert_bytes = (size_t)p.units * p.unit_bytes;
   p.w = w;
   return p;
+}
+
+// Raw-buffer geometry for activation rows of width kmax (bulk copies need 16-byte multiples;
+// scales come by bulk copy only when a row of them is a 16-byte multiple and 16-byte aligned).
+static void set_raw(RowsParams& P, int kind, int kmax, int gmax) {
+  const int ab = kind == TFX_ACT_E4M3 ? 1 : 2;
+  P.raw_row = (kmax * ab + 127) & ~127;
+  P.raw_sc = kind == TFX_ACT_E4M3 ? ((gmax + 15) & ~15) : 0;
 }
 
 size_t packed_gu_bytes(const tfx_dims& d) {
@@ -902,6 +1331,8 @@ extern "C" int tfx_xp_upc_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   P.gu_dbg = gu_dbg;
   P.h_dbg = h_dbg;
   P.gbmax = P.pu.GB;
+  set_raw(P, act_kind, P.pu.K, P.pu.G);
+  P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * P.pu.units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_UPC>(P, mu, 1, max_items, st);
@@ -928,6 +1359,8 @@ extern "C" int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, cons
   P.hs = const_cast<uint8_t*>(h_scale);
   P.out = out;
   P.gbmax = P.pd.GB;
+  set_raw(P, act_kind, P.pd.K, P.pd.G);
+  P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * P.pd.units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_DOWN>(P, 1, md, max_items, st);
@@ -936,7 +1369,7 @@ extern "C" int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, cons
 
 extern "C" size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows) {
   if (!dims_ok(d) || rows < 0) return 0;
-  return sizeof(int32_t) * ((size_t)2 + d.n_experts + (size_t)rows * (d.hidden / 64));
+  return sizeof(int32_t) * ((size_t)2 + d.n_experts + (size_t)rows * (d.hidden / 64));  // see RowsParams
 }
 
 extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
@@ -954,7 +1387,8 @@ extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
     return TFX_EINVAL;
   if (!offs || !active || !n_active || !scratch || (reinterpret_cast<uintptr_t>(scratch) & 3u)) return TFX_EINVAL;
   if (rows == 0) return TFX_OK;
-  if (!ids || !topk_w || !pair_row || !pair_slot || !h || !out || !y || (act_kind == TFX_ACT_E4M3 && !h_scale))
+  if (!ids || !topk_w || !pair_row || !pair_slot || !h || !aligned16(h) || !out || !y ||
+      (act_kind == TFX_ACT_E4M3 && !h_scale))
     return TFX_EINVAL;
   P.ids = ids;
   P.topk_w = topk_w;
@@ -970,7 +1404,10 @@ extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   P.y32 = y_f32_dbg;
   P.scratch = scratch;
   P.gbmax = max(P.pu.GB, P.pd.GB);
-  P.route_ints = 3 * d.n_experts + 2 + 3 * rows * d.top_k + rows;
+  P.route_ints = 3 * d.n_experts + 2 + 3 * rows * d.top_k + rows + 2 * (NTHREADS / 32);
+  set_raw(P, act_kind, max(P.pu.K, P.pd.K), max(P.pu.G, P.pd.G));
+  P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
+  P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * (P.pu.units + P.pd.units);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_FUSED>(P, mu, md, max_items, st);
