@@ -446,9 +446,10 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
     xrow_s[r] = xs_s + xr[r] * GB * 512 + j * 16;
     xmrow_s[r] = xm_s + xr[r] * GB * 8 + j;
   }
-  for (int s = 0; s < pj.S; ++s, ++it) {
-    const int slot = it % NST;
-    const uint32_t ph = (it / NST) & 1u;
+  // ring position, advanced incrementally (no division per stage)
+  int slot = (int)(it % (uint32_t)NST);
+  uint32_t ph = (it / (uint32_t)NST) & 1u;
+  for (int s = 0; s < pj.S; ++s, ++it, slot = slot + 1 == NST ? 0 : slot + 1, ph ^= slot == 0 ? 1u : 0u) {
     if (warp_wait(&B.full[slot], ph, P, abort_flag, dead)) {
       const uint8_t* tile = ring + (size_t)slot * STAGE_B;
       const uint8_t* sc = tile + TROWS * CODE_B;
