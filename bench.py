@@ -27,6 +27,7 @@ sys.path.insert(0, ROOT)
 METRIC = "µs per MoE layer and weight-byte HBM GB/s vs peak at R=1..16 rows"
 UNIT = "us per MoE layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def expert_bytes(H, I):
@@ -45,8 +46,10 @@ def parse():
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling aid: same widths, less memory)")
     ap.add_argument("--eager", action="store_true", help="launch each step from Python instead of graph replay")
-    ap.add_argument("--path", choices=["fused", "separate"], default="fused",
-                    help="fused: one launch per layer (tfx_xp_moe_rows); separate: route, gate/up, down, combine")
+    ap.add_argument("--path", choices=["fused", "separate", "chunk"], default=None,
+                    help="fused: one launch per layer (tfx_xp_moe_rows); separate: route, gate/up, down, combine "
+                         "(rows kernels); chunk: route, gate/up and down on the tensor cores, combine. Default: "
+                         "chunk for the chunk workload, else fused")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -66,18 +69,29 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_hash():
+def tensor_peak_fp8():
+    """Dense E4M3 x E2M1 (kind::mxf8f6f4) tensor peak: the measured bf16 peak times the nominal
+    fp8:bf16 ratio of 2 (4.5 vs 2.25 PFLOP/s dense)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return 2.0 * float(j["bf16_tflops"]), "measured bf16 x 2"
+    return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 2"
+
+
+def kernel_hash(files=("tfx_rows.cu", "tfx_common.cuh")):
     h = hashlib.sha256()
-    for n in ("tfx_rows.cu", "tfx_common.cuh"):
+    for n in files:
         with open(os.path.join(ROOT, "moe_routed_expert_major_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, R, kernel):
-    """dram bytes (read + write) per launch of the timed kernel from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
-    p = os.path.join(ROOT, "profiles", "%s_rows_%s_r%d.md" % (kernel, workload, R))
+def profiled_traffic(name, files=("tfx_rows.cu", "tfx_common.cuh")):
+    """dram bytes (read + write) per launch of the timed kernel from the committed ncu summary
+    profiles/<name>.md, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "%s.md" % name)
     if not os.path.exists(p):
         return None
     src = None
@@ -87,7 +101,7 @@ def profiled_traffic(workload, R, kernel):
             src = line.split(":", 1)[1].strip()
         if line.startswith("dram_bytes_per_launch:"):
             traffic = float(line.split(":", 1)[1].strip())
-    return traffic if src == kernel_hash() else None
+    return traffic if src == kernel_hash(files) else None
 
 
 class Clocks:
@@ -182,12 +196,14 @@ def run_ours(args):
         del dw
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    buf = tfx.alloc_layer(R, H, I, E, k, kind, dev)
+    path = args.path or ("chunk" if args.workload == "chunk" else "fused")
+    chunk = path == "chunk"
+    buf = tfx.alloc_layer(R, H, I, E, k, kind, dev, chunk=chunk)
     n_distinct = len(set(int(e) for e in inp["ids"].ravel()))
     wbytes = n_distinct * expert_bytes(H, I)
     stream = torch.cuda.current_stream()
 
-    fused = args.path == "fused" and R * k <= 256
+    fused = path == "fused" and R * k <= 256
 
     def step(i, ev=None, st=None):
         pk = packed[i % L]
@@ -203,10 +219,17 @@ def run_ours(args):
         tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
         if ev is not None:
             ev[0].record(st)
-        tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+        if chunk:
+            tfx.tfx_xp_upc_chunk(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
+                                 buf["status"])
+        else:
+            tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
         if ev is not None:
             ev[1].record(st)
-        tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        if chunk:
+            tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        else:
+            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
         tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
 
     for i in range(max(3, args.warmup)):
@@ -274,7 +297,7 @@ def run_ours(args):
     status = int(buf["status"].item())
 
     # per-kernel breakdown (diagnostic, outside the timed region)
-    names = ["route", "upc_rows", "down_rows", "combine"]
+    names = ["route", "upc_chunk", "down_chunk", "combine"] if chunk else ["route", "upc_rows", "down_rows", "combine"]
     nb = min(200, K)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
     for i in range(nb):
@@ -283,9 +306,16 @@ def run_ours(args):
         e[0].record(stream)
         tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
         e[1].record(stream)
-        tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+        if chunk:
+            tfx.tfx_xp_upc_chunk(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
+                                 buf["status"])
+        else:
+            tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
         e[2].record(stream)
-        tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        if chunk:
+            tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        else:
+            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
         e[3].record(stream)
         tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
         e[4].record(stream)
@@ -304,7 +334,7 @@ def run_ours(args):
         dx, dxs, dids, dwt = torch.empty_like(x), (torch.empty_like(xs) if xs is not None else None), torch.empty_like(ids), torch.empty_like(w)
         h2d = hx.numel() * hx.element_size() + (hxs.numel() if hxs is not None else 0) + hids.numel() * 4 + hw.numel() * 4
         d2h = hy.numel() * hy.element_size()
-        Ke = min(K, 2000)
+        Ke = min(K, 2000) if not chunk else min(K, 20)
 
         def e2e_step(i):
             dx.copy_(hx, non_blocking=True)
@@ -316,6 +346,13 @@ def run_ours(args):
             if fused:
                 tfx.tfx_xp_moe_rows(d, R, kind, pk, dx, dxs, dids, dwt, buf["route"], buf["h"], buf["h_scale"],
                                     buf["out"], buf["y"], buf["scratch"], buf["status"])
+            elif chunk:
+                tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
+                tfx.tfx_xp_upc_chunk(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
+                                     buf["status"])
+                tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"],
+                                      buf["status"])
+                tfx.tfx_xp_combine(d, R, buf["out"], dwt, buf["y"])
             else:
                 tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
                 tfx.tfx_xp_upc_rows(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
@@ -338,7 +375,8 @@ def run_ours(args):
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_full_layer(cfg, inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds)
+        cpu = cpu_baseline_full_layer(cfg, inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds,
+                                      sample_rows=8 if R > 64 else None)
 
     hbm, hbm_src = peaks()
     kern_avg_ms = statistics.fmean(kern_ms)
@@ -346,15 +384,29 @@ def run_ours(args):
     act_b = 1 if kind == synth.ACT_E4M3 else 2
     x_b = R * H * act_b + (R * (H // 32) if kind == synth.ACT_E4M3 else 0)
     h_b = P * I * act_b + (P * (I // 32) if kind == synth.ACT_E4M3 else 0)
+    tensor = None
     if fused:
         # weights of the distinct experts once, activations in, h written and read back, the
         # expert outputs written and read back by the combine, ids/weights, and y
         kern_name = "moe_rows (route+gate/up+down+combine, one launch)"
         kern_alg = wbytes + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
+    elif chunk:
+        # gate/up weights of the distinct experts once, the activation rows in, h out; the
+        # tensor work is 2 * P * 2I * H flops (E4M3 x E2M1, fp8-class rate)
+        kern_name = "upc_chunk (activation rows into pair order + gate/up chunk kernel, tcgen05 mxf8f6f4)"
+        kern_alg = n_distinct * 2 * I * (H // 2 + H // 32) + x_b + h_b
+        flops = 2.0 * P * 2 * I * H
+        tpeak, tsrc = tensor_peak_fp8()
+        tensor = {"achieved_tflops": round(flops / (kern_avg_ms * 1e-3) / 1e12, 1), "peak_tflops": tpeak,
+                  "peak_source": tsrc, "frac": round(flops / (kern_avg_ms * 1e-3) / 1e12 / tpeak, 4),
+                  "flops_per_launch": flops}
     else:
         kern_name = "upc_rows"
         kern_alg = n_distinct * 2 * I * (H // 2 + H // 32) + x_b + h_b
     achieved = kern_alg / (kern_avg_ms * 1e-3) / 1e9
+    bound = "hbm"
+    if tensor is not None and tensor["flops_per_launch"] / (tensor["peak_tflops"] * 1e12) > kern_alg / (hbm * 1e9):
+        bound = "tensor"
     us_per_layer = 1000.0 * elapsed_ms / (K * world)
     line = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -365,16 +417,21 @@ def run_ours(args):
             "rows": R, "distinct_experts": n_distinct, "weight_bytes_per_layer": wbytes,
             "layers_rotated": L, "l2": "inputs larger than L2: %d packed layer copies rotate (%.0f MB of distinct "
                                         "weights per rotation vs 129 MB L2)" % (L, L * wbytes / 1e6),
-            "path": "fused one-launch layer" if fused else "route + gate/up + down + combine",
+            "path": "fused one-launch layer" if fused else (
+                "route + gate/up chunk + down chunk (tensor cores) + combine" if chunk
+                else "route + gate/up + down + combine"),
             "parallelism": "replicas" if world > 1 else "single GPU"},
         "weight_gbs": round(wbytes / (us_per_layer * 1e-6) / 1e9, 1),
         "weight_gbs_frac_of_peak": round(wbytes / (us_per_layer * 1e-6) / 1e9 / hbm, 4),
         "separate_kernels_us": {n: round(v, 3) for n, v in breakdown.items()},
-        "roofline": {"kernel": kern_name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+        "roofline": {"kernel": kern_name, "bound": bound, "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": hbm_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "algorithmic_bytes_per_launch": int(kern_alg), "avg_launch_us": round(1000 * kern_avg_ms, 3),
-                     "traffic": profiled_traffic(args.workload, R, "fused" if fused else "upc")},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 4) * K, "clocks": clocks,
+                     "traffic": (profiled_traffic("upc_chunk_%s_r%d" % (args.workload, R),
+                                                  ("tfx_chunk.cu", "tfx_common.cuh")) if chunk else
+                                 profiled_traffic("%s_rows_%s_r%d" % ("fused" if fused else "upc", args.workload, R))),
+                     "tensor": tensor},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 5 if chunk else 4) * K, "clocks": clocks,
         "status": status, "launch": "cuda graph replay" if graph is not None else "eager",
     }
     if rank == 0:
@@ -383,10 +440,11 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def _host_layer(cfg, inp, dev):
+def _host_layer(cfg, inp, dev, rows=None):
     import synth
     dw = synth.weights_torch(cfg["E"], cfg["H"], cfg["I"], cfg["seed"], dev)
-    experts = sorted(set(int(e) for e in inp["ids"].ravel()))
+    ids = inp["ids"] if rows is None else inp["ids"][rows]
+    experts = sorted(set(int(e) for e in ids.ravel() if 0 <= int(e) < cfg["E"]))
     lay = dict(H=cfg["H"], I=cfg["I"], E=cfg["E"], k=cfg["k"], kind=cfg["kind"])
     for n, t in dw.items():
         full = {}
@@ -405,24 +463,32 @@ class _ExpertDict:
         return self.d[int(e)]
 
 
-def cpu_baseline_full_layer(cfg, inp, packed_seed, dev, seconds):
-    """The oracle (fp32-chain mode, as it stands) on whole layers of the same workload."""
+def cpu_baseline_full_layer(cfg, inp, packed_seed, dev, seconds, sample_rows=None):
+    """The oracle (fp32-chain mode, as it stands) on whole layers of the same workload, or, for
+    a large layer, on its first `sample_rows` rows, scaled to the layer by the row count."""
     import oracle
-    lay = _host_layer(cfg, inp, dev)
     R, k = inp["ids"].shape
-    threads = min(os.cpu_count() or 1, R * k)
+    rows = None if sample_rows is None else list(range(min(sample_rows, R)))
+    lay = _host_layer(cfg, inp, dev, rows=rows)
+    threads = min(os.cpu_count() or 1, R * k if rows is None else len(rows) * k)
     oracle.layer_chain(lay, threads=threads, rows=[0])  # load and warm the library
     n = 0
     t = time.perf_counter()
     while True:
-        oracle.layer_chain(lay, threads=threads)
+        oracle.layer_chain(lay, threads=threads, rows=rows)
         n += 1
         el = time.perf_counter() - t
         if el >= seconds or n >= 50:
             break
-    return {"value": round(1e6 * el / n, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d whole %s layer(s) (route, %d gate/up + SwiGLU + quantiser + down pairs, combine), "
-                      "fp32-chain mode, pairs spread over %d host threads" % (n, cfg["name"], R * k, threads)}
+    per = el / n
+    if rows is None:
+        return {"value": round(1e6 * per, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+                "sample": "%d whole %s layer(s) (route, %d gate/up + SwiGLU + quantiser + down pairs, combine), "
+                          "fp32-chain mode, pairs spread over %d host threads" % (n, cfg["name"], R * k, threads)}
+    return {"value": round(1e6 * per * R / len(rows), 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "rows 0-%d of the %s layer (%d pairs: gate/up + SwiGLU + quantiser + down, combine) %d "
+                      "time(s), fp32-chain mode over %d host threads, scaled by %d/%d rows" % (
+                          len(rows) - 1, cfg["name"], len(rows) * k, n, threads, R, len(rows))}
 
 
 # ------------------------------------------------------------------------------- reference

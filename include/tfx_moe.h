@@ -153,6 +153,49 @@ int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* 
                      const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
                      const tfx_rows_opts* opts, void* stream);
 
+/* ---------------------------------------------------------------- chunk path (tensor cores)
+ * The same two operations as tfx_xp_upc_rows and tfx_xp_down_rows, for launches with many
+ * rows per expert (a prompt chunk: 4,096 rows route about 128 rows to each of 256 experts).
+ * The page keeps prompt chunks on their own, chunk-invariant kernels. Here each expert's
+ * gate/up and down are dense block-scaled contractions on the tensor cores: tcgen05.mma
+ * kind::mxf8f6f4, with E4M3 activations x E2M1 weights, one E8M0 scale per 32 k on each
+ * side, and fp32 accumulation in tensor memory. A tile is 128 pairs of one expert x 256
+ * weight rows, streamed 128 k at a time.
+ *
+ * Numerics. The accumulation order is the tensor cores' own, not the fixed fp32 chain of
+ * the _rows entries, so the two paths are separate invariance domains: the caller picks one,
+ * and nothing switches between them implicitly.
+ *   - Every pair's results are independent of the other pairs in the launch. They are
+ *     bit-identical whether the row runs alone or in any chunk.
+ *   - g, u, h (before quantisation) and d are within 1e-3 * sum|terms| + 1e-6 of float64.
+ *   - SwiGLU runs in fp32 with the fast exponential and division (g / (1 + e^-g) * u); the
+ *     E4M3 quantiser of h is that of tfx_xp_upc_rows.
+ *
+ * Arguments, layouts and outputs are those of the _rows entries, plus a workspace for gate/up.
+ *   - ws: tfx_xp_upc_chunk_ws_bytes(d, R) bytes of device memory, 256-byte aligned, owned by
+ *     the caller; the call first copies the activation rows (and scales) into pair order
+ *     there, so that each tile's rows are one TMA box. Its contents are scratch.
+ *   - TFX_EUNSUPPORTED: bf16 activations; H or I not a multiple of 512.
+ *   - Alignment: packed and out 32-byte aligned; x, h, x_scale and h_scale 16-byte aligned;
+ *     gu_dbg and h_dbg (when given) 16-byte aligned.
+ *   - opts: only timeout_ns is read.
+ *
+ * Resources. One CTA per SM runs persistently over the tiles. Each CTA holds about 214 KB of
+ * shared memory and all 512 columns of its SM's tensor memory for the duration of the launch.
+ * Operands arrive by TMA (the packed weights through a tensor map that expands E2M1 into the
+ * tensor cores' 16-byte slots, the activation rows and their scales by four-row gathers). The first call
+ * looks up cuTensorMapEncodeTiled through the runtime (cudaGetDriverEntryPointByVersion);
+ * TFX_ECUDA if the driver does not provide it.
+ * Waits are bounded (TFX_ST_TIMEOUT). */
+size_t tfx_xp_upc_chunk_ws_bytes(tfx_dims d, int32_t rows);
+int tfx_xp_upc_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                     const uint8_t* x_scale, const tfx_route* rt, void* h, uint8_t* h_scale, float* gu_dbg,
+                     float* h_dbg, void* ws, size_t ws_bytes, int32_t* status, const tfx_rows_opts* opts,
+                     void* stream);
+int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* h,
+                      const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
+                      const tfx_rows_opts* opts, void* stream);
+
 /* ---------------------------------------------------------------- whole layer, one launch
  * Route, gate/up, down and combine of a small launch (R*k <= 256 routed pairs: decode) in a
  * single kernel launch, with the same results, bit for bit, as tfx_xp_route followed by

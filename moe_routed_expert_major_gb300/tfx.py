@@ -57,6 +57,11 @@ def load():
                                                ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_down_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, ctypes.POINTER(Route), _P, _P,
                                                 ctypes.POINTER(RowsOpts), _P]),
+            "tfx_xp_upc_chunk_ws_bytes": (ctypes.c_size_t, [Dims, _I32]),
+            "tfx_xp_upc_chunk": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, ctypes.POINTER(Route), _P, _P, _P, _P, _P,
+                                                ctypes.c_size_t, _P, ctypes.POINTER(RowsOpts), _P]),
+            "tfx_xp_down_chunk": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, ctypes.POINTER(Route), _P, _P,
+                                                ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_combine": (ctypes.c_int, [Dims, _I32, _P, _P, _P, _P, _P]),
             "tfx_xp_moe_rows_scratch_bytes": (ctypes.c_size_t, [Dims, _I32]),
             "tfx_xp_moe_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -137,6 +142,28 @@ def tfx_xp_down_rows(d, rows, kind, packed, h, h_scale, rt, out, status, opts=No
                                    _ptr(status), o, _stream()), "tfx_xp_down_rows")
 
 
+def tfx_xp_upc_chunk_ws_bytes(d, rows):
+    return int(load().tfx_xp_upc_chunk_ws_bytes(d, rows))
+
+
+def tfx_xp_upc_chunk(d, rows, kind, packed, x, x_scale, rt, h, h_scale, ws, status, gu_dbg=None, h_dbg=None,
+                     opts=None):
+    r = route_struct(rt)
+    o = ctypes.byref(opts) if opts is not None else None
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().tfx_xp_upc_chunk(d, rows, kind, _ptr(packed), _ptr(x), _ptr(x_scale), ctypes.byref(r), _ptr(h),
+                                   _ptr(h_scale), _ptr(gu_dbg), _ptr(h_dbg), _ptr(ws), nbytes, _ptr(status), o,
+                                   _stream()),
+           "tfx_xp_upc_chunk")
+
+
+def tfx_xp_down_chunk(d, rows, kind, packed, h, h_scale, rt, out, status, opts=None):
+    r = route_struct(rt)
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(load().tfx_xp_down_chunk(d, rows, kind, _ptr(packed), _ptr(h), _ptr(h_scale), ctypes.byref(r), _ptr(out),
+                                    _ptr(status), o, _stream()), "tfx_xp_down_chunk")
+
+
 def tfx_xp_combine(d, rows, out, topk_w, y, y_f32=None):
     _check(load().tfx_xp_combine(d, rows, _ptr(out), _ptr(topk_w), _ptr(y), _ptr(y_f32), _stream()),
            "tfx_xp_combine")
@@ -179,8 +206,9 @@ def alloc_route(R, E, k, device):
                 active=torch.zeros(max(min(R * k, E), 1), **i32), n_active=torch.zeros(1, **i32))
 
 
-def alloc_layer(R, H, I, E, k, kind, device, debug=False):
-    """Output and intermediate buffers of one layer launch of R rows."""
+def alloc_layer(R, H, I, E, k, kind, device, debug=False, chunk=False):
+    """Output and intermediate buffers of one layer launch of R rows (chunk=True adds the gate/up
+    chunk path's workspace)."""
     P = max(R * k, 1)
     b = dict(route=alloc_route(R, E, k, device), status=torch.zeros(1, dtype=torch.int32, device=device))
     if kind == ACT_E4M3:
@@ -193,6 +221,10 @@ def alloc_layer(R, H, I, E, k, kind, device, debug=False):
     b["y"] = torch.empty(max(R, 1), H, dtype=torch.int16, device=device)
     nsc = tfx_xp_moe_rows_scratch_bytes(Dims(H, I, E, k), max(R, 1)) // 4
     b["scratch"] = torch.zeros(max(nsc, 1), dtype=torch.int32, device=device)
+    b["chunk_ws"] = None
+    if chunk:
+        b["chunk_ws"] = torch.empty(max(tfx_xp_upc_chunk_ws_bytes(Dims(H, I, E, k), R), 1), dtype=torch.uint8,
+                                    device=device)
     if debug:
         b["gu_dbg"] = torch.empty(P, 2, I, dtype=torch.float32, device=device)
         b["h_dbg"] = torch.empty(P, I, dtype=torch.float32, device=device)
@@ -206,6 +238,16 @@ def layer_fused(d, R, kind, packed, x, x_scale, ids, w, buf, opts=None):
     """One MoE layer of R rows in a single launch (tfx_xp_moe_rows)."""
     tfx_xp_moe_rows(d, R, kind, packed, x, x_scale, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
                     buf["y"], buf["scratch"], buf["status"], buf["y_f32"], opts)
+
+
+def layer_chunk(d, R, kind, packed, x, x_scale, ids, w, buf, opts=None):
+    """One MoE layer of R rows on the chunk path: route -> gate/up chunk -> down chunk ->
+    combine, four launches on the current stream."""
+    tfx_xp_route(d, R, ids, buf["route"], buf["status"])
+    tfx_xp_upc_chunk(d, R, kind, packed, x, x_scale, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
+                     buf["status"], buf["gu_dbg"], buf["h_dbg"], opts)
+    tfx_xp_down_chunk(d, R, kind, packed, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"], opts)
+    tfx_xp_combine(d, R, buf["out"], w, buf["y"], buf["y_f32"])
 
 
 def layer_rows(d, R, kind, packed, x, x_scale, ids, w, buf, opts_upc=None, opts_down=None):

@@ -78,6 +78,25 @@ def run_layer(lay, packed, debug=True, opts_upc=None, opts_down=None, canary=Non
     return res
 
 
+def run_layer_chunk(lay, packed, debug=True, canary=None):
+    """Route + gate/up + down on the chunk path (tensor cores) + combine; numpy results."""
+    R, k = lay["ids"].shape
+    d = tfx.dims(lay["H"], lay["I"], lay["E"], k)
+    xd, xs, ids, w = to_dev_inputs(lay)
+    buf = tfx.alloc_layer(R, lay["H"], lay["I"], lay["E"], k, lay["kind"], DEV, debug=debug, chunk=True)
+    if canary is not None:
+        for n in ("h", "h_scale", "out", "y", "gu_dbg", "h_dbg", "y_f32"):
+            if buf.get(n) is not None:
+                buf[n].view(torch.uint8).fill_(canary)
+    tfx.layer_chunk(d, R, lay["kind"], packed, xd, xs, ids, w, buf)
+    torch.cuda.synchronize()
+    res = {n: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for n, v in buf.items()
+           if n not in ("route", "chunk_ws")}
+    res["route"] = {n: v.cpu().numpy() for n, v in buf["route"].items()}
+    res["status"] = int(buf["status"].item())
+    return res
+
+
 def h_in_from_gpu(lay, res):
     """The device's quantised h, keyed by (row, slot), for the oracle's down stage."""
     rt = res["route"]

@@ -70,3 +70,30 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
     assert L.tfx_xp_pack(bad, st, st, st, st, st, st, st, None) == -1
     assert L.tfx_selftest_wait_timeout(None, 1000, None) == -1
     assert L.tfx_strerror(-2) == b"unsupported shape for these kernels"
+
+
+def test_chunk_entries_reject_before_launch(lib):
+    """The chunk path covers E4M3 activations with H and I multiples of 512 only."""
+    from moe_routed_expert_major_gb300 import tfx
+    d = tfx.dims(7168, 2048, 256, 8)
+    st = ctypes.c_void_p(64)  # aligned for every argument
+    rt = tfx.Route(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16))
+    L = lib
+    big = 1 << 40
+    up = lambda dd, kind, x=st, xs=st, r=ctypes.byref(rt), ws=ctypes.c_void_p(256), wsb=big: L.tfx_xp_upc_chunk(
+        dd, 4, kind, st, x, xs, r, st, st, None, None, ws, wsb, st, None, None)
+    assert up(d, 1) == -2                         # bf16 activations
+    assert up(tfx.dims(7168 + 256, 2048, 256, 8), 0) == -2  # H not a multiple of 512
+    assert up(tfx.dims(7168, 2048 + 128, 256, 8), 0) == -2  # I not a multiple of 512
+    assert up(tfx.dims(7168, 2048, 0, 8), 0) == -1
+    assert up(d, 0, x=ctypes.c_void_p(24)) == -1  # x not 16-byte aligned
+    assert up(d, 0, xs=ctypes.c_void_p(72)) == -1  # x_scale not 16-byte aligned
+    assert up(d, 0, r=None) == -1
+    assert L.tfx_xp_upc_chunk(d, 4, 0, ctypes.c_void_p(16), st, st, ctypes.byref(rt), st, st, None, None,
+                              ctypes.c_void_p(256), big, st, None, None) == -1  # packed not 32-byte aligned
+    assert up(d, 0, ws=None) == -1                       # no workspace
+    assert up(d, 0, wsb=L.tfx_xp_upc_chunk_ws_bytes(d, 4) - 1) == -1  # workspace too small
+    assert L.tfx_xp_upc_chunk_ws_bytes(d, 4096) == 32768 * 7168 + 32768 * 224
+    assert L.tfx_xp_down_chunk(d, 4, 0, st, st, st, ctypes.byref(rt), None, st, None, None) == -1
+    assert L.tfx_xp_down_chunk(d, 4, 1, st, st, st, ctypes.byref(rt), st, st, None, None) == -2
+    assert L.tfx_xp_down_chunk(d, 0, 0, st, st, st, ctypes.byref(rt), st, st, None, None) == 0  # R = 0: no-op
