@@ -1,33 +1,38 @@
 // tfx_chunk.cu -- the many-rows-per-expert (prompt chunk) path. Gate/up and down of every
-// routed pair run as a dense block-scaled contraction on the fifth-generation tensor cores:
-// tcgen05.mma kind::mxf8f6f4 with E4M3 activations (operand A, one routed pair per row) and
-// E2M1 weights (operand B, one weight row per column), one E8M0 scale per 32 k on each side,
-// fp32 accumulators in tensor memory. The same maths as the rows kernels, reached through
-// the tensor cores' own summation order instead of the fixed fma chain: results are within
-// the float64 tolerance, and every pair's bits are independent of which other pairs share
-// its launch (the instruction shape, the k order and the pair's operands are the same
-// whatever the chunk; only its lane changes).
+// routed pair run as dense block-scaled contractions on the fifth-generation tensor cores:
+// tcgen05.mma kind::mxf8f6f4 with E2M1 weights (operand A: 128 weight rows, K-major) and E4M3
+// activations (operand B: the expert's routed pairs, K-major), one E8M0 scale per 32 k on each
+// side, fp32 accumulators in tensor memory. The same maths as the rows kernels, reached
+// through the tensor cores' own summation order instead of the fixed fma chain: results are
+// within the float64 tolerance, and every pair's bits are independent of which other pairs
+// share its launch (the pair's operands and the k order are the same whatever the chunk; the
+// pair only changes column).
 //
 // Source: "dsv41 metal: decode experts decode an expert's weights once for all of its rows"
 // (TensorFold PR #2983), which keeps prompt chunks on their own chunk-invariant kernels. A
 // 4,096-row chunk routes about 128 rows to each expert, so gate/up and down there are dense
 // contractions close to the HBM/tensor ridge.
 //
+// Tiles. A tile is one expert's block of up to CK_NMAX routed pairs (the MMA's N, rounded up
+// to 16, so an expert's pairs are not padded to a power of two) against 256 weight rows, as
+// two accumulators of 128 lanes:
+//   gate/up: accumulator 0 = the 128 gate rows of four packed units (n = 32 u0 .. 32 u0 + 127),
+//            accumulator 1 = the 128 up rows of the same n: lane l of both holds the same n,
+//            so SwiGLU is thread-local and a warp's 32 lanes are one quantisation group;
+//   down:    accumulator 0 = m0 .. m0 + 127, accumulator 1 = m0 + 128 .. m0 + 255.
+// Each pipeline stage carries 128 k: two MMAs (one per accumulator) for each K = 32 step.
+//
 // CTA roles (448 threads, one CTA per SM, persistent over tiles):
 //   warps 0-3, 10-13  epilogue: tensor memory -> registers -> SwiGLU + quantiser (gate/up) or
-//              d rows (down). A warp reads the lanes of its quadrant (warp % 4: pairs
-//              32 (warp % 4) .. + 31 of the tile); warps 0-3 take accumulator columns 0-127,
-//              warps 10-13 columns 128-255.
-//   warps 4-7  scale movers: each thread owns one pair row of the tile; once a stage has
-//              landed it writes both scale sets of the stage into tensor memory
+//              d (down). A warp reads the lanes of its quadrant (warp % 4); warps 0-3 take the
+//              even 16-column chunks of the tile's pairs, warps 10-13 the odd ones.
+//   warps 4-7  scale movers: once a stage has landed, write its weight-row and pair scales
+//              into tensor memory (tcgen05.st, each warp its own lane quadrant)
 //   warp 8     allocates tensor memory and issues the MMAs (one lane)
-//   warp 9     TMA (one lane): the weight tile (E2M1 expanded into 16-byte slots by the
-//              tensor map's 16U4_ALIGN16B type), the weight scales (bulk copies), the tile's
-//              activation rows and their scales. Activations are read in pair order (h for
-//              down; for gate/up a copy of x gathered into pair order first), so a tile's 128
-//              rows are one box. The operands land 128B-swizzled.
-// A tile is 128 routed pairs of one expert x 256 weight rows (four packed units); each
-// pipeline stage carries 128 k (four MMAs of K = 32).
+//   warp 9     TMA (one lane): the weight rows (E2M1 expanded into 16-byte slots by the tensor
+//              map's 16U4_ALIGN16B type) and their scales, and the pairs' activation rows and
+//              scales in pair order (h for down; for gate/up a copy of x gathered into pair
+//              order first), one box each. Operands land 128B-swizzled.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -41,38 +46,40 @@ size_t packed_gu_bytes(const tfx_dims& d);
 
 namespace {
 
-constexpr int CK_M = 128;        // routed pairs per tile (MMA M: tensor-memory lanes)
-constexpr int CK_N = 256;        // weight rows per tile (MMA N: accumulator columns)
+constexpr int CK_M = 128;        // weight rows per accumulator (MMA M: tensor-memory lanes)
+constexpr int CK_NMAX = 160;     // routed pairs per tile at most (MMA N, a multiple of 16)
 constexpr int CK_KT = 128;       // k per pipeline stage
 constexpr int CK_NS = 4;         // pipeline stages
 constexpr int CK_THREADS = 448;  // 8 epilogue + 4 scale-mover warps + MMA warp + TMA warp
 constexpr int CK_EPI_WARPS = 8;
-// Shared memory: a ring of CK_NS stages (weights, then activations; both 128B-swizzled,
-// 1024-byte aligned), then two buffers of scales. Scales come once per packed stage (512 k,
-// four ring stages): every buffer holds all 16 groups of the packed stage, for the weight
-// rows ([4 units][64 rows][16]) and for the tile's pairs ([128][16]).
-constexpr int CK_B_OFF = 0;          // 32,768: E2M1 weights, 8 code bytes per 16-byte slot
-constexpr int CK_A_OFF = 32768;      // 16,384: E4M3 activations
-constexpr int CK_STAGE = 49152;      // 48 x 1024
-constexpr int CK_SB_BYTES = 4096;    // weight scales of one packed stage
-constexpr int CK_SA_BYTES = 2048;    // pair scales of one packed stage
-constexpr int CK_SC_BUF = CK_SB_BYTES + CK_SA_BYTES;
-constexpr uint32_t CK_TX = 16384 + 16384;                // bytes of every stage's copies
-constexpr uint32_t CK_TX_SC = CK_SB_BYTES + 128 * 16;    // plus, at a packed stage's first stage, its scales
+// A stage: the two weight-row operands, then the pair operand (all 128B-swizzled, 1024-byte
+// aligned). Scales come once per packed stage (512 k = four ring stages) into one of two
+// buffers: the four units' weight-row scales as packed ([4][64 rows][16 groups]) and the
+// tile's pair scales ([pair][16 groups]).
+constexpr int CK_A0_OFF = 0;         // 16,384: 128 weight rows, E2M1 in 16-byte slots
+constexpr int CK_A1_OFF = 16384;     // 16,384
+constexpr int CK_B_OFF = 32768;      // 20,480: up to 160 pairs x 128 bytes, E4M3
+constexpr int CK_STAGE = 53248;      // 52 x 1024
+constexpr int CK_SW_BYTES = 4096;    // weight-row scales of one packed stage
+constexpr int CK_SP_BYTES = CK_NMAX * 16;  // pair scales of one packed stage
+constexpr int CK_SC_BUF = CK_SW_BYTES + CK_SP_BYTES;
 constexpr int CK_TMEM_COLS = 512;
-constexpr int CK_SF_COL = 256;   // scale columns of stage s: 256 + 12 s (A: 4, B: 8)
+constexpr int CK_D1_COL = CK_NMAX;   // accumulator 1 (accumulator 0 at column 0)
+constexpr int CK_SF_COL = 2 * CK_NMAX;  // scale columns of stage s: 320 + 16 s (A0: 4, A1: 4, B: 8)
+static_assert(CK_SF_COL + 16 * CK_NS <= CK_TMEM_COLS, "tensor memory");
+static_assert(CK_NMAX % 32 == 0 && CK_NMAX <= 256, "pair boxes of 32");
 // packed weight layout (tfx_pack.cu): stages of 64 rows x 256 code bytes, then 64 x 16 scales
 constexpr int PK_STAGE_BYTES = 64 * (256 + 16), PK_CODE_BYTES = 64 * 256;
 
 struct ChunkParams {
   int K, G;          // contraction width (H for gate/up, I for down) and its 32-groups
-  int ntn;           // weight-row tiles of 256 (2I/256 or H/256)
+  int nwb;           // 256-row weight blocks of the projection (I/128 for gate/up, H/256 for down)
+  int units;         // packed units per expert
   int E, k, R, P, I, H;
   int down;
   const uint8_t* w;  // packed projection
   size_t unit_bytes, expert_bytes;
-  const uint8_t* x;  // activation rows: x [R][H] (gate/up, by pair_row) or h [P][I] (down, by pair)
-  const uint8_t* xs; // their E8M0 scales [rows][K/32]
+  const uint8_t* xs; // activation scales in pair order [P][K/32] (for the tensor map)
   const int32_t *offs, *pair_row, *pair_slot, *active, *n_active;
   uint8_t* h;
   uint8_t* hs;
@@ -84,10 +91,10 @@ struct ChunkParams {
 };
 
 struct Tile {
-  int e, p0, mreal, u0;  // expert, first pair, pairs (<= 128), first packed unit of the weight rows
+  int e, p0, np, u0;  // expert, first pair, pairs (<= CK_NMAX), first packed unit of the weight block
 };
 
-// ------------------------------------------------------------------ tcgen05 / cp.async wrappers
+// ------------------------------------------------------------------ tcgen05 / TMA wrappers
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -113,11 +120,11 @@ __device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* tm, int c0,
       "l"(tm), "r"(c0), "r"(c1), "r"(smem_addr(bar))
       : "memory");
 }
-// Instruction descriptor of kind::mxf8f6f4 with block scaling: A E4M3 (0), B E2M1 (5), both
-// K-major, E8M0 scales, M = 128, N = 256; sf_id picks the byte of the scale words.
-__device__ __forceinline__ uint32_t mma_idesc(uint32_t sf_id) {
-  return (sf_id & 3u) << 4 | 0u << 7 | 5u << 10 | (uint32_t)(CK_N >> 3) << 17 | 1u << 23 |
-         (uint32_t)(CK_M >> 4) << 24 | (sf_id & 3u) << 29;
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A E2M1 (5), B E4M3 (0), both
+// K-major, E8M0 scales, M = 128, N = n; sf_id picks the byte of the scale words.
+__device__ __forceinline__ uint32_t mma_idesc(uint32_t n, uint32_t sf_id) {
+  return (sf_id & 3u) << 4 | 5u << 7 | 0u << 10 | (n >> 3) << 17 | 1u << 23 | (uint32_t)(CK_M >> 4) << 24 |
+         (sf_id & 3u) << 29;
 }
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                           uint32_t sfb, uint32_t accumulate) {
@@ -160,8 +167,12 @@ __device__ __forceinline__ bool ck_wait(uint64_t* bar, uint32_t parity, const Ch
   return true;
 }
 
-// Tile t of this launch: tiles are numbered expert by expert (active order), then by
-// weight-row tile, then by 128-pair block, so concurrent CTAs share experts in L2.
+// Pair blocks of an expert with ne pairs: as many blocks of at most CK_NMAX as needed, sizes
+// as equal as possible.
+__device__ __forceinline__ int pair_blocks(int ne) { return (ne + CK_NMAX - 1) / CK_NMAX; }
+
+// Tile t of this launch: tiles are numbered expert by expert (active order), then by pair
+// block, then by weight block, so that concurrent CTAs share an expert's pairs and weights in L2.
 __device__ __forceinline__ bool tile_of(const ChunkParams& P, const int* tpre, int n_act, int t, int& a,
                                         Tile& T) {
   while (a < n_act && tpre[a + 1] <= t) ++a;
@@ -170,22 +181,23 @@ __device__ __forceinline__ bool tile_of(const ChunkParams& P, const int* tpre, i
   if (e < 0 || e >= P.E) return false;
   const int p0 = P.offs[e], ne = P.offs[e + 1] - p0;
   if (ne <= 0 || p0 < 0 || p0 + ne > P.P) return false;
-  const int mtn = (ne + CK_M - 1) / CK_M;
+  const int nb = pair_blocks(ne);
   const int local = t - tpre[a];
-  const int nt = local / mtn, mt = local - nt * mtn;
+  const int pb = local / P.nwb, wb = local - pb * P.nwb;
+  const int base = ne / nb, rem = ne - base * nb;
   T.e = e;
-  T.p0 = p0 + CK_M * mt;
-  T.mreal = min(CK_M, ne - CK_M * mt);
-  T.u0 = nt * (CK_N / 64);
+  T.p0 = p0 + pb * base + min(pb, rem);
+  T.np = base + (pb < rem ? 1 : 0);
+  T.u0 = 4 * wb;
   return true;
 }
 
 __global__ void __launch_bounds__(CK_THREADS, 1)
-    chunk_kernel(const ChunkParams P, const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                 const __grid_constant__ CUtensorMap tm_xs) {
+    chunk_kernel(const ChunkParams P, const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_ws,
+                 const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xs) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);  // 1024-byte aligned ring
-  uint8_t* scbuf = smem + CK_NS * CK_STAGE;  // [2][weight scales | pair scales]
+  uint8_t* scbuf = smem + CK_NS * CK_STAGE;  // [2][weight-row scales | pair scales]
   uint64_t* full_tma = reinterpret_cast<uint64_t*>(scbuf + 2 * CK_SC_BUF);
   uint64_t* full_sc = full_tma + CK_NS;
   uint64_t* empty = full_sc + CK_NS;
@@ -226,7 +238,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
         const int e = P.active[a];
         if (e >= 0 && e < P.E) {
           const int ne = P.offs[e + 1] - P.offs[e];
-          if (ne > 0) t = P.ntn * ((ne + CK_M - 1) / CK_M);
+          if (ne > 0) t = P.nwb * pair_blocks(ne);
         }
       }
       int inc = t;
@@ -258,8 +270,9 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
     for (int t = blockIdx.x; t < total && !dead; t += gridDim.x) {
       Tile T;
       if (!tile_of(P, tpre, n_act, t, a_hint, T)) continue;
-      const int wunit = T.e * (P.ntn * (CK_N / 64)) + T.u0;  // packed unit index (expert-major)
-      const uint8_t* wexp = P.w + (size_t)T.e * P.expert_bytes;
+      const int ub = T.e * P.units + T.u0;  // packed unit index of the block (expert-major)
+      const uint32_t tx = 2u * 8192u + (uint32_t)CK_NMAX * 128u;  // weight halves (packed bytes) + pair box
+      const uint32_t tx_sc = (uint32_t)(CK_SW_BYTES + CK_SP_BYTES);
       for (int ks = 0; ks < nks; ++ks) {
         if (it >= (uint32_t)CK_NS &&
             !__all_sync(0xffffffffu, ck_wait(&empty[slot], ph ^ 1u, P, abort))) {
@@ -271,16 +284,19 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
         const bool first = kin == 0;  // a packed stage starts: bring its scales too
         uint8_t* sc = scbuf + ((it >> 2) & 1u) * CK_SC_BUF;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&full_tma[slot], CK_TX + (first ? CK_TX_SC : 0u));
-          tma_4d(st + CK_B_OFF, &tm_w, kin, 0, ps, wunit, &full_tma[slot]);
-          tma_2d(st + CK_A_OFF, &tm_x, k0, T.p0, &full_tma[slot]);  // rows past the pairs read as zero
+          mbar_arrive_expect_tx(&full_tma[slot], tx + (first ? tx_sc : 0u));
+          if (!P.down) {  // 32 gate rows of each of the four units, then their 32 up rows
+            tma_4d(st + CK_A0_OFF, &tm_w, kin, 0, ps, ub, &full_tma[slot]);
+            tma_4d(st + CK_A1_OFF, &tm_w, kin, 32, ps, ub, &full_tma[slot]);
+          } else {        // units u0, u0+1 (m0 .. m0+127), then u0+2, u0+3
+            tma_4d(st + CK_A0_OFF, &tm_w, kin, 0, ps, ub, &full_tma[slot]);
+            tma_4d(st + CK_A1_OFF, &tm_w, kin, 0, ps, ub + 2, &full_tma[slot]);
+          }
+          // the tile's pairs (rows past them are read, as zero past the end, and not used)
+          tma_2d(st + CK_B_OFF, &tm_x, k0, T.p0, &full_tma[slot]);
           if (first) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              bulk_g2s(sc + 1024 * c,
-                       wexp + (size_t)(T.u0 + c) * P.unit_bytes + (size_t)ps * PK_STAGE_BYTES + PK_CODE_BYTES, 1024,
-                       &full_tma[slot]);
-            tma_2d(sc + CK_SB_BYTES, &tm_xs, 16 * ps, T.p0, &full_tma[slot]);
+            tma_4d(sc, &tm_ws, 0, 0, ps, T.e * P.units + T.u0, &full_tma[slot]);
+            tma_2d(sc + CK_SW_BYTES, &tm_xs, 16 * ps, T.p0, &full_tma[slot]);
           }
         }
         __syncwarp();
@@ -298,13 +314,17 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
     __syncwarp();
   } else if (warp >= 4 && warp < 8) {
     // ---------------------------------------------------------------- scale movers
-    const int tp = tid - 128, q = warp - 4;
+    const int q = warp - 4;
     const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
     uint32_t it = 0;
     int slot = 0;
     uint32_t ph = 0;
     bool dead = false;
     int a_hint = 0;
+    // weight row of lane (q, lane) in each accumulator: gate/up: unit u0+q, rows lane (gate)
+    // and 32+lane (up); down: unit u0+q/2 (+2), row 32 (q&1) + lane
+    const int w0 = P.down ? 1024 * (q >> 1) + (32 * (q & 1) + lane) * 16 : 1024 * q + lane * 16;
+    const int w1 = P.down ? 1024 * (2 + (q >> 1)) + (32 * (q & 1) + lane) * 16 : 1024 * q + (32 + lane) * 16;
     for (int t = blockIdx.x; t < total && !dead; t += gridDim.x) {
       Tile T;
       if (!tile_of(P, tpre, n_act, t, a_hint, T)) continue;
@@ -315,14 +335,19 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
         }
         const uint8_t* sc = scbuf + ((it >> 2) & 1u) * CK_SC_BUF;
         const int g4 = ((ks * CK_KT) & 511) >> 5;  // first of the stage's 4 groups within the packed stage
-        const uint32_t sa = *reinterpret_cast<const uint32_t*>(sc + CK_SB_BYTES + 16 * tp + g4);
+        const uint32_t sa0 = *reinterpret_cast<const uint32_t*>(sc + w0 + g4);
+        const uint32_t sa1 = *reinterpret_cast<const uint32_t*>(sc + w1 + g4);
         uint32_t sb[8];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)  // weight row 32 c + lane: unit c/2, row 32 (c&1) + lane
-          sb[c] = *reinterpret_cast<const uint32_t*>(sc + 1024 * (c >> 1) + (32 * (c & 1) + lane) * 16 + g4);
-        const uint32_t col = CK_SF_COL + 12 * slot;
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tq + col + q), "r"(sa) : "memory");
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tq + col + 4),
+        for (int c = 0; c < 8; ++c) {  // pair column 32 c + lane (columns past CK_NMAX: scale 1)
+          const int n = 32 * c + lane;
+          sb[c] = n < CK_NMAX ? *reinterpret_cast<const uint32_t*>(sc + CK_SW_BYTES + 16 * n + g4) : 0x7F7F7F7Fu;
+        }
+        const uint32_t col = CK_SF_COL + 16 * slot;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tq + col + q), "r"(sa0) : "memory");
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tq + col + 4 + q), "r"(sa1)
+                     : "memory");
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tq + col + 8),
                      "r"(sb[0]), "r"(sb[1]), "r"(sb[2]), "r"(sb[3]), "r"(sb[4]), "r"(sb[5]), "r"(sb[6]), "r"(sb[7])
                      : "memory");
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -339,7 +364,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
   } else if (warp == 8) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
-      uint32_t it = 0, ntile = 0;
+      uint32_t ntile = 0;
       int slot = 0;
       uint32_t ph = 0;
       int a_hint = 0;
@@ -347,6 +372,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
       for (int t = blockIdx.x; t < total && !dead; t += gridDim.x) {
         Tile T;
         if (!tile_of(P, tpre, n_act, t, a_hint, T)) continue;
+        const uint32_t n16 = (uint32_t)((T.np + 15) & ~15);
         if (ntile > 0 && !ck_wait(acc_empty, (ntile - 1) & 1u, P, abort)) break;
         tc_fence_after();
         for (int ks = 0; ks < nks; ++ks) {
@@ -356,13 +382,16 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
           }
           tc_fence_after();
           const uint8_t* st = smem + slot * CK_STAGE;
-          const uint32_t sfa = tmem + CK_SF_COL + 12 * slot, sfb = sfa + 4;
+          const uint32_t sf = tmem + CK_SF_COL + 16 * slot;
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            mma_issue(tmem, smem_desc_sw128(st + CK_A_OFF + 32 * u), smem_desc_sw128(st + CK_B_OFF + 32 * u),
-                      mma_idesc((uint32_t)u), sfa, sfb, (ks | u) != 0);
+          for (int u = 0; u < 4; ++u) {
+            const uint64_t bd = smem_desc_sw128(st + CK_B_OFF + 32 * u);
+            const uint32_t id = mma_idesc(n16, (uint32_t)u);
+            mma_issue(tmem, smem_desc_sw128(st + CK_A0_OFF + 32 * u), bd, id, sf, sf + 8, (ks | u) != 0);
+            mma_issue(tmem + CK_D1_COL, smem_desc_sw128(st + CK_A1_OFF + 32 * u), bd, id, sf + 4, sf + 8,
+                      (ks | u) != 0);
+          }
           mma_commit(&empty[slot]);
-          ++it;
           if (++slot == CK_NS) {
             slot = 0;
             ph ^= 1u;
@@ -380,8 +409,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
   } else {
     // ---------------------------------------------------------------- epilogue (warps 0-3, 10-13)
     const int qd = warp & 3, half = warp >= 10 ? 1 : 0;
-    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16) + 128 * half;
-    const int m = 32 * qd + lane;
+    const uint32_t tq = tmem + ((uint32_t)(32 * qd) << 16);
     uint32_t ntile = 0;
     int a_hint = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -389,93 +417,81 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
       if (!tile_of(P, tpre, n_act, t, a_hint, T)) continue;
       if (!__all_sync(0xffffffffu, ck_wait(acc_full, ntile & 1u, P, abort))) break;
       tc_fence_after();
-      const bool valid = m < T.mreal;
-      const int p = T.p0 + m;
-      if (!P.down) {
-        const int I = P.I;
-#pragma unroll 1
-        for (int jj = 0; jj < 2; ++jj) {  // packed unit u0 + j: 32 gate columns, then the 32 up columns
-          const int j = 2 * half + jj;
-          float g[32], u[32];
-          tmem_ld16(tq + 64 * jj, *reinterpret_cast<float(*)[16]>(g));
-          tmem_ld16(tq + 64 * jj + 16, *reinterpret_cast<float(*)[16]>(g + 16));
-          tmem_ld16(tq + 64 * jj + 32, *reinterpret_cast<float(*)[16]>(u));
-          tmem_ld16(tq + 64 * jj + 48, *reinterpret_cast<float(*)[16]>(u + 16));
-          const int n0 = 32 * (T.u0 + j);
-          float hv[32];
-          bool bad = false;
-          uint32_t amax_b = 0u;
+      // this warp's pair columns: chunks of 16, alternating between the two halves
+      const int nch = (T.np + 15) >> 4;
+      // down: (row, slot) of this warp's pairs, fetched at once (lane l < 16 of chunk slot ci
+      // holds pair 16 (half + 2 ci) + l)
+      int rsv[(CK_NMAX / 16 + 1) / 2];
+      if (P.down) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
+        for (int ci = 0; ci < (CK_NMAX / 16 + 1) / 2; ++ci) {
+          const int j = 16 * (half + 2 * ci) + lane;
+          rsv[ci] = -1;
+          if (lane < 16 && j < T.np) {
+            const int p = T.p0 + j;
+            const int row = P.pair_row[p], sl = P.pair_slot[p];
+            rsv[ci] = (row >= 0 && row < P.R && sl >= 0 && sl < P.k) ? row * P.k + sl : -2;
+          }
+        }
+      }
+      for (int ch = half; ch < nch; ch += 2) {
+        const int c0 = 16 * ch;
+        float a[16], b[16];
+        tmem_ld16(tq + c0, a);
+        tmem_ld16(tq + CK_D1_COL + c0, b);
+        if (!P.down) {
+          const int I = P.I;
+          const int n = 32 * (T.u0 + qd) + lane;  // this lane's output n (gate in a, up in b)
+          float hv[16];
+          uint32_t amax[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
             // silu(g) * u with the fast exponential and division: the chunk path is held to
             // the float64 bound, not to the rows path's bits
-            hv[c] = __fdividef(g[c], 1.0f + __expf(-g[c])) * u[c];
-            bad |= isnan(hv[c]) || isinf(hv[c]);
-            amax_b = max(amax_b, __float_as_uint(fabsf(hv[c])));
+            hv[c] = __fdividef(a[c], 1.0f + __expf(-a[c])) * b[c];
+            amax[c] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));  // NaN/Inf: >= 0x7F800000
           }
-          if (valid) {
-            if (P.gu_dbg) {
-              float* gd = P.gu_dbg + (size_t)p * 2 * I + n0;
 #pragma unroll
-              for (int c = 0; c < 32; c += 4) {
-                *reinterpret_cast<float4*>(gd + c) = make_float4(g[c], g[c + 1], g[c + 2], g[c + 3]);
-                *reinterpret_cast<float4*>(gd + I + c) = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
-              }
-            }
-            if (P.h_dbg) {
-              float* hd = P.h_dbg + (size_t)p * I + n0;
-#pragma unroll
-              for (int c = 0; c < 32; c += 4)
-                *reinterpret_cast<float4*>(hd + c) = make_float4(hv[c], hv[c + 1], hv[c + 2], hv[c + 3]);
-            }
+          for (int c = 0; c < 16; ++c) {
+            const int j = c0 + c;
+            const uint32_t amax_b = amax[c];
+            const bool bad = amax_b >= 0x7F800000u;
             uint32_t sc;
             if (bad) sc = 255u;
             else if (amax_b == 0u) sc = 127u;
             else {
-              const int e2 =
-                  amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
+              const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
               sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
             }
-            const float rs = e8m0_recip_f32(sc);
-            uint32_t wv[8];
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-              uint32_t w = 0;
-#pragma unroll
-              for (int b = 0; b < 4; ++b) {
-                const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv[4 * c4 + b], rs));
-                w |= code << (8 * b);
+            const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv[c], e8m0_recip_f32(sc)));
+            if (j < T.np) {
+              const int p = T.p0 + j;
+              P.h[(size_t)p * I + n] = (uint8_t)code;
+              if (lane == 0) P.hs[(size_t)p * (I / 32) + T.u0 + qd] = (uint8_t)sc;
+              if (P.gu_dbg) {
+                P.gu_dbg[(size_t)p * 2 * I + n] = a[c];
+                P.gu_dbg[(size_t)p * 2 * I + I + n] = b[c];
               }
-              wv[c4] = w;
+              if (P.h_dbg) P.h_dbg[(size_t)p * I + n] = hv[c];
             }
-            uint4* hp = reinterpret_cast<uint4*>(P.h + (size_t)p * I + n0);
-            hp[0] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            hp[1] = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-            P.hs[(size_t)p * (I / 32) + T.u0 + j] = (uint8_t)sc;
           }
-        }
-      } else {
-        int row = -1, slot = -1;
-        if (valid) {
-          row = P.pair_row[p];
-          slot = P.pair_slot[p];
-          if (row < 0 || row >= P.R || slot < 0 || slot >= P.k) {
-            report(P.status, TFX_ST_SHAPE);
-            row = -1;
-          }
-        }
-        float* dst = row >= 0 ? P.out + ((size_t)row * P.k + slot) * P.H + 64 * T.u0 + 128 * half : nullptr;
-#pragma unroll 1
-        for (int j = 0; j < CK_N / 32; ++j) {
-          float v[16];
-          tmem_ld16(tq + 16 * j, v);
-          if (dst) {  // whole 32-byte sectors, not kept in L1 (the combine reads d much later)
+        } else {
+          // lane holds m = m0 + 32 qd + lane (a) and m + 128 (b); d of pair j goes to out[row][slot]
+          const int m = 64 * T.u0 + 32 * qd + lane;
+          int rs = -1;
 #pragma unroll
-            for (int c = 0; c < 16; c += 8)
-              asm volatile("st.global.L1::no_allocate.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst + 16 * j + c),
-                           "f"(v[c]), "f"(v[c + 1]), "f"(v[c + 2]), "f"(v[c + 3]), "f"(v[c + 4]), "f"(v[c + 5]),
-                           "f"(v[c + 6]), "f"(v[c + 7])
-                           : "memory");
+          for (int ci = 0; ci < (CK_NMAX / 16 + 1) / 2; ++ci)
+            if (half + 2 * ci == ch) rs = rsv[ci];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int r = __shfl_sync(0xffffffffu, rs, c);
+            if (r >= 0) {
+              float* dst = P.out + (size_t)r * P.H + m;
+              __stcs(dst, a[c]);
+              __stcs(dst + 128, b[c]);
+            } else if (r == -2 && lane == 0) {
+              report(P.status, TFX_ST_SHAPE);
+            }
           }
         }
       }
@@ -494,7 +510,7 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
 
 // Gate/up activations in pair order: xp[p] = x[pair_row[p]] and xsp[p] = xs[pair_row[p]] for
 // the routed pairs p < offs[E] (one warp per pair, 16-byte copies), so that the chunk kernel
-// loads a tile's 128 rows as one box.
+// loads a tile's pairs as 32-row boxes.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* __restrict__ x, const uint8_t* __restrict__ xs,
                                                           const int32_t* __restrict__ pair_row,
                                                           const int32_t* __restrict__ offs, int E, int R, int H, int G,
@@ -537,30 +553,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Tensor maps of one launch: the packed projection's codes as a 4-D tensor of E2M1 values
-// (512 k of a stage row, 64 rows, stages, experts x units), loaded as 128 k x 64 rows x 4
-// units boxes into 16-byte slots; the activation rows in pair order [pairs][K] (bytes) as
-// 128 k x 128 pair boxes (both 128-byte swizzled); their scales [pairs][K/32] as 16 x 128
-// boxes.
-int encode_maps(const ChunkParams& P, int nrows, CUtensorMap* tw, CUtensorMap* tx, CUtensorMap* txs) {
+// (512 k of a stage row, 64 rows, stages, experts x units), loaded as 128 k boxes of 32 rows x
+// 4 units (gate/up: the gate or the up halves) or 64 rows x 2 units (down), expanded into
+// 16-byte slots; the same rows' scales (16 groups x 64 rows x 4 units per box); the
+// activation rows in pair order [pairs][K] (bytes) as 128 k x CK_NMAX pair boxes (these and
+// the weights 128-byte swizzled); their scales [pairs][K/32] as 16 x CK_NMAX boxes.
+int encode_maps(const ChunkParams& P, const void* x, int nrows, CUtensorMap* tw, CUtensorMap* tws, CUtensorMap* tx,
+                CUtensorMap* txs) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) return TFX_ECUDA;
   const int S = (P.K + 511) / 512;
-  const cuuint64_t units = (cuuint64_t)P.E * (cuuint64_t)(P.ntn * (CK_N / 64));
-  const cuuint64_t gdw[4] = {512, 64, (cuuint64_t)S, units};
+  const cuuint64_t gdw[4] = {512, 64, (cuuint64_t)S, (cuuint64_t)P.E * (cuuint64_t)P.units};
   const cuuint64_t gsw[3] = {256, (cuuint64_t)PK_STAGE_BYTES, (cuuint64_t)P.unit_bytes};
-  const cuuint32_t bw[4] = {128, 64, 1, 4}, es[4] = {1, 1, 1, 1};
-  if (enc(tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(P.w), gdw, gsw, bw, es,
+  const cuuint32_t bw_gu[4] = {128, 32, 1, 4}, bw_d[4] = {128, 64, 1, 2}, es[4] = {1, 1, 1, 1};
+  if (enc(tw, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, const_cast<uint8_t*>(P.w), gdw, gsw, P.down ? bw_d : bw_gu, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return TFX_EINVAL;
+  // the weight rows' scales: 16 groups of a stage row, 64 rows, stages, experts x units
+  const cuuint64_t gdws[4] = {16, 64, (cuuint64_t)S, (cuuint64_t)P.E * (cuuint64_t)P.units};
+  const cuuint64_t gsws[3] = {16, (cuuint64_t)PK_STAGE_BYTES, (cuuint64_t)P.unit_bytes};
+  const cuuint32_t bws[4] = {16, 64, 1, 4};
+  if (enc(tws, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(P.w) + PK_CODE_BYTES, gdws, gsws, bws, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return TFX_EINVAL;
   const cuuint64_t gdx[2] = {(cuuint64_t)P.K, (cuuint64_t)nrows}, gsx[1] = {(cuuint64_t)P.K};
-  const cuuint32_t bx[2] = {128, CK_M};
-  if (enc(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(P.x), gdx, gsx, bx, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+  const cuuint32_t bx[2] = {128, CK_NMAX};
+  if (enc(tx, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(x), gdx, gsx, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+      CUDA_SUCCESS)
     return TFX_EINVAL;
   const cuuint64_t gds[2] = {(cuuint64_t)P.G, (cuuint64_t)nrows}, gss[1] = {(cuuint64_t)P.G};
-  const cuuint32_t bs[2] = {16, CK_M};
+  const cuuint32_t bs[2] = {16, CK_NMAX};
   if (enc(txs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(P.xs), gds, gss, bs, es,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
@@ -568,7 +593,7 @@ int encode_maps(const ChunkParams& P, int nrows, CUtensorMap* tw, CUtensorMap* t
   return TFX_OK;
 }
 
-int chunk_launch(const ChunkParams& P, int nrows, cudaStream_t st) {
+int chunk_launch(const ChunkParams& P, const void* x, int nrows, cudaStream_t st) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))
     return TFX_ECUDA;
@@ -580,10 +605,10 @@ int chunk_launch(const ChunkParams& P, int nrows, cudaStream_t st) {
       return TFX_ELAUNCH;
     configured[dev] = (int)smem;
   }
-  alignas(64) CUtensorMap tw, tx, txs;
-  const int rc = encode_maps(P, nrows, &tw, &tx, &txs);
+  alignas(64) CUtensorMap tw, tws, tx, txs;
+  const int rc = encode_maps(P, x, nrows, &tw, &tws, &tx, &txs);
   if (rc) return rc;
-  chunk_kernel<<<sms, CK_THREADS, smem, st>>>(P, tw, tx, txs);
+  chunk_kernel<<<sms, CK_THREADS, smem, st>>>(P, tw, tws, tx, txs);
   return cudaGetLastError() == cudaSuccess ? TFX_OK : TFX_ELAUNCH;
 }
 
@@ -619,11 +644,11 @@ void set_proj(const tfx_dims& d, bool down, const uint8_t* packed, ChunkParams& 
   P.K = down ? d.inter : d.hidden;
   P.G = P.K / 32;
   const int S = (P.K + 511) / 512;
-  const int units = down ? d.hidden / 64 : d.inter / 32;
+  P.units = down ? d.hidden / 64 : d.inter / 32;
   P.unit_bytes = (size_t)S * PK_STAGE_BYTES;
-  P.expert_bytes = (size_t)units * P.unit_bytes;
+  P.expert_bytes = (size_t)P.units * P.unit_bytes;
   P.w = down ? packed + packed_gu_bytes(d) : packed;
-  P.ntn = (down ? d.hidden : 2 * d.inter) / CK_N;
+  P.nwb = P.units / 4;
 }
 
 }  // namespace
@@ -659,13 +684,12 @@ extern "C" int tfx_xp_upc_chunk(tfx_dims d, int32_t rows, int32_t act_kind, cons
   gather_rows_kernel<<<4 * sms, 256, 0, st>>>(static_cast<const uint8_t*>(x), x_scale, rt->pair_row, rt->offs, d.n_experts,
                                                rows, d.hidden, d.hidden / 32, P.P, xp, xsp);
   if (cudaGetLastError() != cudaSuccess) return TFX_ELAUNCH;
-  P.x = xp;
   P.xs = xsp;
   P.h = static_cast<uint8_t*>(h);
   P.hs = h_scale;
   P.gu_dbg = gu_dbg;
   P.h_dbg = h_dbg;
-  return chunk_launch(P, P.P, st);
+  return chunk_launch(P, xp, P.P, st);
 }
 
 extern "C" int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* h,
@@ -675,10 +699,9 @@ extern "C" int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, con
   const int rc = chunk_common(d, rows, act_kind, packed, rt, status, opts, P);
   if (rc) return rc;
   if (rows == 0) return TFX_OK;
-  if (!h || !h_scale || !out || !al(h, 16) || !al(h_scale, 16) || !al(out, 32)) return TFX_EINVAL;
+  if (!h || !h_scale || !out || !al(h, 16) || !al(h_scale, 16) || !al(out, 16)) return TFX_EINVAL;
   set_proj(d, true, packed, P);
-  P.x = static_cast<const uint8_t*>(h);
   P.xs = h_scale;
   P.out = out;
-  return chunk_launch(P, rows * d.top_k, static_cast<cudaStream_t>(stream));
+  return chunk_launch(P, h, P.P, static_cast<cudaStream_t>(stream));
 }
