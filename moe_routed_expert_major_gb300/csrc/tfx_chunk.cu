@@ -138,18 +138,16 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// Issues the load of 16 columns of this warp's 32 lanes; the registers are valid after tmem_wait().
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Bounded wait that also gives up once another role has aborted the CTA.
 __device__ __forceinline__ bool ck_wait(uint64_t* bar, uint32_t parity, const ChunkParams& P, volatile int* abort) {
@@ -434,21 +432,20 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
           }
         }
       }
-      for (int ch = half; ch < nch; ch += 2) {
+      // one 16-column chunk of both accumulators, already in registers
+      auto proc = [&](const uint32_t (&ra)[16], const uint32_t (&rb)[16], int ch) {
         const int c0 = 16 * ch;
-        float a[16], b[16];
-        tmem_ld16(tq + c0, a);
-        tmem_ld16(tq + CK_D1_COL + c0, b);
         if (!P.down) {
           const int I = P.I;
-          const int n = 32 * (T.u0 + qd) + lane;  // this lane's output n (gate in a, up in b)
+          const int n = 32 * (T.u0 + qd) + lane;  // this lane's output n (gate in ra, up in rb)
           float hv[16];
           uint32_t amax[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             // silu(g) * u with the fast exponential and division: the chunk path is held to
             // the float64 bound, not to the rows path's bits
-            hv[c] = __fdividef(a[c], 1.0f + __expf(-a[c])) * b[c];
+            const float g = __uint_as_float(ra[c]);
+            hv[c] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(rb[c]);
             amax[c] = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));  // NaN/Inf: >= 0x7F800000
           }
 #pragma unroll
@@ -469,14 +466,14 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
               P.h[(size_t)p * I + n] = (uint8_t)code;
               if (lane == 0) P.hs[(size_t)p * (I / 32) + T.u0 + qd] = (uint8_t)sc;
               if (P.gu_dbg) {
-                P.gu_dbg[(size_t)p * 2 * I + n] = a[c];
-                P.gu_dbg[(size_t)p * 2 * I + I + n] = b[c];
+                P.gu_dbg[(size_t)p * 2 * I + n] = __uint_as_float(ra[c]);
+                P.gu_dbg[(size_t)p * 2 * I + I + n] = __uint_as_float(rb[c]);
               }
               if (P.h_dbg) P.h_dbg[(size_t)p * I + n] = hv[c];
             }
           }
         } else {
-          // lane holds m = m0 + 32 qd + lane (a) and m + 128 (b); d of pair j goes to out[row][slot]
+          // lane holds m = m0 + 32 qd + lane (ra) and m + 128 (rb); d of pair j goes to out[row][slot]
           const int m = 64 * T.u0 + 32 * qd + lane;
           int rs = -1;
 #pragma unroll
@@ -487,12 +484,36 @@ __global__ void __launch_bounds__(CK_THREADS, 1)
             const int r = __shfl_sync(0xffffffffu, rs, c);
             if (r >= 0) {
               float* dst = P.out + (size_t)r * P.H + m;
-              __stcs(dst, a[c]);
-              __stcs(dst + 128, b[c]);
+              __stcs(dst, __uint_as_float(ra[c]));
+              __stcs(dst + 128, __uint_as_float(rb[c]));
             } else if (r == -2 && lane == 0) {
               report(P.status, TFX_ST_SHAPE);
             }
           }
+        }
+      };
+      // this warp's chunks are half, half + 2, ...: loads run one chunk ahead of the
+      // processing, alternating between two register sets
+      uint32_t xa[16], xb[16], ya[16], yb[16];
+      if (half < nch) {
+        tmem_ld16_issue(tq + 16 * half, xa);
+        tmem_ld16_issue(tq + CK_D1_COL + 16 * half, xb);
+      }
+      tmem_wait();
+      for (int ch = half; ch < nch; ch += 4) {
+        if (ch + 2 < nch) {  // warp-uniform
+          tmem_ld16_issue(tq + 16 * (ch + 2), ya);
+          tmem_ld16_issue(tq + CK_D1_COL + 16 * (ch + 2), yb);
+        }
+        proc(xa, xb, ch);
+        tmem_wait();
+        if (ch + 2 < nch) {
+          if (ch + 4 < nch) {
+            tmem_ld16_issue(tq + 16 * (ch + 4), xa);
+            tmem_ld16_issue(tq + CK_D1_COL + 16 * (ch + 4), xb);
+          }
+          proc(ya, yb, ch + 2);
+          tmem_wait();
         }
       }
       tc_fence_before();

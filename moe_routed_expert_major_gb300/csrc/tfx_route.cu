@@ -8,7 +8,9 @@
 // offsets and the active list. Phase 3: each warp walks its chunk in rounds of 32 pairs; a
 // pair's position is its (warp, expert) base plus its rank among the round's pairs of the
 // same expert (__match_any_sync), so every expert's pairs come out in ascending
-// (row, slot) order whatever the thread timing.
+// (row, slot) order whatever the thread timing. When the ids fit, the kernel first copies them
+// into shared memory (coalesced) and records each pair's validity there, so that neither the
+// duplicate checks nor the scatter go back to global memory.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -29,17 +31,23 @@ __device__ __forceinline__ int pair_expert(const int32_t* ids, int q, int k, int
   return e;
 }
 
-__global__ void __launch_bounds__(RT_THREADS) route_kernel(const int32_t* __restrict__ ids, int P, int k, int E,
+template <bool STAGED>
+__global__ void __launch_bounds__(RT_THREADS) route_kernel(const int32_t* __restrict__ ids_g, int P, int k, int E,
                                                            int32_t* offs, int32_t* pair_row, int32_t* pair_slot,
                                                            int32_t* active, int32_t* n_active, int32_t* status) {
-  extern __shared__ int hist[];  // [RT_WARPS][E], then scan scratch [E]
+  extern __shared__ int hist[];  // [RT_WARPS][E], then scan scratch [E]; staged: ids [P], valid [P] bytes
   int* eoff = hist + RT_WARPS * E;
+  int* s_ids = eoff + E;
+  uint8_t* s_valid = reinterpret_cast<uint8_t*>(s_ids + (STAGED ? P : 0));
   __shared__ int s_bad;
   __shared__ int s_nact;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < RT_WARPS * E; i += RT_THREADS) hist[i] = 0;
+  if (STAGED)
+    for (int i = tid; i < P; i += RT_THREADS) s_ids[i] = ids_g[i];
   if (tid == 0) { s_bad = 0; s_nact = 0; }
   __syncthreads();
+  const int32_t* ids = STAGED ? s_ids : ids_g;
 
   const int chunk = (P + RT_WARPS - 1) / RT_WARPS;
   const int c0 = min(P, warp * chunk), c1 = min(P, c0 + chunk);
@@ -47,6 +55,7 @@ __global__ void __launch_bounds__(RT_THREADS) route_kernel(const int32_t* __rest
   // phase 1: per-warp histogram
   for (int q = c0 + lane; q < c1; q += 32) {
     const int e = pair_expert(ids, q, k, E, &bad);
+    if (STAGED) s_valid[q] = e >= 0 ? 1 : 0;
     if (e >= 0) atomicAdd(&hist[warp * E + e], 1);
   }
   if (bad) atomicOr(&s_bad, bad);
@@ -99,7 +108,8 @@ __global__ void __launch_bounds__(RT_THREADS) route_kernel(const int32_t* __rest
   for (int q0 = c0; q0 < c1; q0 += 32) {
     const int q = q0 + lane;
     int dummy = 0;
-    const int e = q < c1 ? pair_expert(ids, q, k, E, &dummy) : -1;
+    int e = -1;
+    if (q < c1) e = STAGED ? (s_valid[q] ? ids[q] : -1) : pair_expert(ids, q, k, E, &dummy);
     const unsigned peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const int leader = __ffs(peers) - 1;
@@ -125,8 +135,13 @@ extern "C" int tfx_xp_route(tfx_dims d, int32_t rows, const int32_t* ids, int32_
   if (!offs || !active || !n_active || !status) return TFX_EINVAL;
   if (rows > 0 && (!ids || !pair_row || !pair_slot)) return TFX_EINVAL;
   const int E = d.n_experts;
-  const size_t smem = (size_t)(RT_WARPS + 1) * E * sizeof(int);
-  auto kern = route_kernel;
+  const int P = rows * d.top_k;
+  // ids staged in shared memory (4 bytes + 1 validity byte per pair) when they fit
+  const size_t base = (size_t)(RT_WARPS + 1) * E * sizeof(int);
+  const size_t staged = base + (size_t)P * 5 + 16;
+  const bool stage = P > 0 && staged <= 200 * 1024;
+  const size_t smem = stage ? staged : base;
+  auto kern = stage ? route_kernel<true> : route_kernel<false>;
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return TFX_ELAUNCH;
