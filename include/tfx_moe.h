@@ -208,7 +208,9 @@ int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t*
  * ids int32 [R][k], topk_w fp32 [R][k]; h / h_scale / out as for the separate entries; y bf16
  * [R][H]; y_f32_dbg fp32 [R][H] or NULL.
  * scratch: tfx_xp_moe_rows_scratch_bytes(d, R) bytes of device memory, 4-byte aligned, zero
- * before its first use; every call returns it to zero, so calls sharing one scratch buffer
+ * before its first use; every call that completes returns it to zero (each counter's last
+ * user clears it; a call that stopped early on TFX_ST_TIMEOUT may leave counters set, and the
+ * caller then zeroes the buffer before the next call), so calls sharing one scratch buffer
  * must not overlap on the device. The CTAs of one launch wait on one another, so the launch
  * is cooperative (all CTAs resident at once; the runtime refuses it otherwise: TFX_ELAUNCH);
  * a wait that runs out sets TFX_ST_TIMEOUT.

@@ -24,7 +24,7 @@
 //     memory in every CTA, runs all gate/up items, then the down items (each waits, bounded,
 //     for its expert's gate/up items), and combines each (row, 64-output block) in the CTA
 //     whose down item completes the row's last slot. Completion counters live in caller
-//     scratch, which the last CTA to finish returns to zero.
+//     scratch; each counter's last user returns it to zero (no end-of-launch barrier).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -82,8 +82,9 @@ struct RowsParams {
   float* out;           // [R][k][H]
   uint16_t* y;          // fused: [R][H] bf16
   float* y32;           // fused: [R][H] or null
-  int32_t* scratch;     // fused: [0] exit count, [1] work counter, [2..E+1] gate/up items done
-                        //        per active expert, then [R][H/64] slots written per (row, block)
+  int32_t* scratch;     // fused: [0] unused, [1] work counter, [2..E+1] gate/up items done per
+                        //        active expert, [E+2..2E+1] down items past their wait per active
+                        //        expert, then [R][H/64] slots written per (row, block)
   int32_t* status;
   int tier_mode;
   uint64_t timeout_ns;
@@ -634,6 +635,7 @@ __device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars&
             if (lane == 0) last = atomicAdd(&slots_done[(size_t)row * P.pd.units + q.u], 1) == r_rowcnt[row] - 1;
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
+              if (lane == 0) slots_done[(size_t)row * P.pd.units + q.u] = 0;  // last user of the counter
               __threadfence();
 #pragma unroll
               for (int hh = 0; hh < 2; ++hh) {
@@ -817,7 +819,8 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
   sc.offs = r_offs;
   int32_t* work_ctr = PH == PH_FUSED ? P.scratch + 1 : nullptr;
   int32_t* done_upc = PH == PH_FUSED ? P.scratch + 2 : nullptr;
-  int32_t* slots_done = PH == PH_FUSED ? P.scratch + 2 + P.E : nullptr;
+  int32_t* down_seen = PH == PH_FUSED ? P.scratch + 2 + P.E : nullptr;
+  int32_t* slots_done = PH == PH_FUSED ? P.scratch + 2 + 2 * P.E : nullptr;
   int* qid = reinterpret_cast<int*>(smem + Ly.ctrl + 16);  // [QD] claimed item ids
   PassGen gen = {};
   PassDesc d;
@@ -851,8 +854,18 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
           if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
           *abort_flag = 1;
         } else if (!*abort_flag) {
-          // a CTA's first item is its own index; the counter hands out the rest
-          v = claims == 0 ? (int)blockIdx.x : atomicAdd(work_ctr, 1) + (int)gridDim.x;
+          // A CTA's first item is its own index; the counter hands out the rest. Every CTA
+          // with a first item claims once more than it gets, so the launch makes exactly
+          // max(0, total - grid) + min(total, grid) counter claims; the last one returns the
+          // counter to zero for the next launch.
+          if (claims == 0) {
+            v = (int)blockIdx.x;
+          } else {
+            const int raw = atomicAdd(work_ctr, 1);
+            const int g = (int)gridDim.x;
+            if (raw == max(0, sc.total - g) + min(sc.total, g) - 1) *work_ctr = 0;
+            v = raw + g;
+          }
           if (v >= sc.total) v = -1;
         }
         qid[slot] = v;
@@ -951,6 +964,11 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
           __nanosleep(64);
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read next by the async proxy
+        // the expert's last down item past this point returns both counters to zero
+        if (okw && atomicAdd(down_seen + q.a, 1) == P.pd.units - 1) {
+          done_upc[q.a] = 0;
+          down_seen[q.a] = 0;
+        }
       }
       if (!__shfl_sync(0xffffffffu, okw, 0)) dead = true;
     };
@@ -1088,22 +1106,6 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
                                                   xm_s, prow, xraw, d.real, it, dead, ep);
       else dispatch_pass<KIND, MAXR_U, false>(d.t, P, pj, ring, B, bx, be, eph, d.pidx >= 2, abort_flag, xs_s,
                                               xm_s, prow, xraw, d.real, it, dead, ep);
-    }
-  }
-  if (PH == PH_FUSED) {
-    // the last CTA to finish returns the counters to zero for the next launch
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const int prev = atomicAdd(P.scratch, 1);
-      if (prev == (int)gridDim.x - 1) {
-        __threadfence();
-        for (int i = 1; i <= P.E + 1; ++i) P.scratch[i] = 0;
-        const int nc = P.R * P.pd.units;
-        for (int i = 0; i < nc; ++i) slots_done[i] = 0;
-        __threadfence();
-        P.scratch[0] = 0;
-      }
     }
   }
 }
@@ -1370,7 +1372,7 @@ extern "C" int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, cons
 
 extern "C" size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows) {
   if (!dims_ok(d) || rows < 0) return 0;
-  return sizeof(int32_t) * ((size_t)2 + d.n_experts + (size_t)rows * (d.hidden / 64));  // see RowsParams
+  return sizeof(int32_t) * ((size_t)2 + 2 * (size_t)d.n_experts + (size_t)rows * (d.hidden / 64));  // see RowsParams
 }
 
 extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
