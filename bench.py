@@ -60,6 +60,17 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(value, world):
+    """The largest of every rank's value (the job's time is its slowest rank's); one rank: the value."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -300,10 +311,7 @@ def run_ours(args):
             graph_ev.replay()
         torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in kev]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world)
     status = int(buf["status"].item())
 
     # per-kernel breakdown (diagnostic, outside the timed region)
