@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "shared", "apart", "chunk"])
     ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--act", choices=["e4m3", "bf16"], default=None,
+                    help="override the workload's activation format")
     ap.add_argument("--layers", type=int, default=4)
     ap.add_argument("--experts", type=int, default=None, help="override E (profiling aid: same widths, less memory)")
     ap.add_argument("--eager", action="store_true", help="launch each step from Python instead of graph replay")
@@ -185,6 +187,8 @@ def run_ours(args):
     over = {} if args.rows is None else {"R": args.rows}
     if args.experts is not None:
         over["E"] = args.experts
+    if args.act is not None:
+        over["kind"] = synth.ACT_E4M3 if args.act == "e4m3" else synth.ACT_BF16
     cfg = synth.workload(args.workload, **over)
     H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
     d = tfx.dims(H, I, E, k)
@@ -534,6 +538,8 @@ def run_reference(args):
     if rank != 0:
         return
     over = {} if args.rows is None else {"R": args.rows}
+    if args.act is not None:
+        over["kind"] = synth.ACT_E4M3 if args.act == "e4m3" else synth.ACT_BF16
     cfg = synth.workload(args.workload, **over)
     H, I, k, R, kind = cfg["H"], cfg["I"], cfg["k"], cfg["R"], cfg["kind"]
     inp = synth.make_inputs(cfg)

@@ -205,84 +205,69 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const
       }
     }
   } else {
-    // bf16: a half-warp converts one 32-group (two values a lane) with a power-of-two shift
-    // 2^sigma that maps the group's largest magnitude into [2^15, 2^16). The group is exact in
-    // f16 and its chain equals the unshifted fp32 chain times 2^sigma when every finite nonzero
-    // value has exponent in [e_max - 32, e_max], e_max <= 119 and e_min >= -141 (products and
-    // partial sums then stay in fp32's normal range, or on its subnormal grid, on both sides).
+    // bf16: one thread converts one 32-group with a power-of-two shift 2^sigma that maps the
+    // group's largest magnitude into [2^15, 2^16). The group is exact in f16 and its chain
+    // equals the unshifted fp32 chain times 2^sigma when every finite nonzero value has
+    // exponent in [e_max - 32, e_max], e_max <= 119 and e_min >= -141 (products and partial
+    // sums then stay in fp32's normal range, or on its subnormal grid, on both sides).
     // Otherwise the multiplier is 0 and the exact fallback runs for that group.
-    const int wp = tid >> 5, half = (tid >> 4) & 1, lane16 = tid & 15;
     const int gall = GB * 8;
     const int total = real * gall;
-    const int step = NT / 16;
-    for (int ib = 2 * wp; ib < total; ib += BATCH * step) {  // uniform trip count per warp
-      uint32_t tw[BATCH];
+    for (int i = tid; i < total; i += NT) {
+      const int r = i / gall, g = i - r * gall;
+      uint4 v[4];  // the group's 32 bf16 values, element 2j in the low half of word j
 #pragma unroll
-      for (int q = 0; q < BATCH; ++q) {
-        const int i = ib + q * step + half;
-        tw[q] = 0u;
-        if (i < total) {
-          const int r = i / gall, g = i - r * gall;
-          if (g < G) {
-            const uint8_t* src = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride + 2 * (32 * g + 2 * lane16);
-            tw[q] = FROM_SMEM ? *reinterpret_cast<const uint32_t*>(src)
-                              : __ldcg(reinterpret_cast<const unsigned int*>(src));
-          }
-        }
+      for (int q = 0; q < 4; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G) {
+        const uint8_t* src = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride + 64 * g;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          v[q] = FROM_SMEM ? *reinterpret_cast<const uint4*>(src + 16 * q)
+                           : __ldcg(reinterpret_cast<const uint4*>(src + 16 * q));
       }
+      const uint32_t* wv = reinterpret_cast<const uint32_t*>(v);
+      int emax = -1000, emin = 1000;
 #pragma unroll
-      for (int q = 0; q < BATCH; ++q) {
-        const int i = ib + q * step + half;
-        const bool act = i < total;
-        const uint32_t two = tw[q];
-        int r = 0, g = 0;
-        if (act) {
-          r = i / gall;
-          g = i - r * gall;
-        }
-        int emax = -1000, emin = 1000;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t bb = (two >> (16 * hh)) & 0xFFFFu;
-          const uint32_t ef = (bb >> 7) & 0xFFu, m = bb & 0x7Fu;
-          if (ef == 255u || (ef == 0u && m == 0u)) continue;  // NaN/Inf or zero
-          const int e = ef ? (int)ef - 127 : (31 - __clz((int)m)) - 133;
-          emax = max(emax, e);
-          emin = min(emin, e);
-        }
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) {
-          emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-          emin = min(emin, __shfl_xor_sync(0xffffffffu, emin, o));
-        }
-        if (!act) continue;
-        int sigma = 0;
-        bool safe = true;
-        if (emax > -1000) {
-          sigma = 15 - emax;
-          safe = (emax <= 119) && (emin >= -141) && (emax - emin <= 32);
-        }
-        float lo = __uint_as_float(two << 16), hi = __uint_as_float(two & 0xFFFF0000u);
-        if (safe) {
-          const int s1 = min(max(sigma, -126), 127), s2 = sigma - s1;  // 2^sigma as two exact factors
-          const float f1 = __uint_as_float((uint32_t)(127 + s1) << 23);
-          const float f2 = __uint_as_float((uint32_t)(127 + s2) << 23);
-          lo = __fmul_rn(__fmul_rn(lo, f1), f2);
-          hi = __fmul_rn(__fmul_rn(hi, f1), f2);
-        }
-        const __half2 h2 = __floats2half2_rn(lo, hi);
-        const int t = 2 * lane16;
-        *reinterpret_cast<__half2*>(xs_s + xoff(r, g, t >> 3, GB) + ((t & 7) << 1)) = h2;
-        if (lane16 == 0) {
-          float m = 0.0f;  // 0 marks the exact fallback
-          if (g >= G) m = 1.0f;
-          else if (safe) {
-            const int ns = -sigma;  // 2^-sigma, possibly subnormal (exact)
-            m = ns >= -126 ? __uint_as_float((uint32_t)(127 + ns) << 23) : __uint_as_float(0x00400000u >> (-127 - ns));
-          }
-          xm_s[r * gall + g] = m;
-        }
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t bb = (wv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        const uint32_t ef = (bb >> 7) & 0xFFu, m = bb & 0x7Fu;
+        const bool skip = ef == 255u || (ef == 0u && m == 0u);  // NaN/Inf or zero
+        const int e = ef ? (int)ef - 127 : (31 - __clz((int)m)) - 133;
+        emax = skip ? emax : max(emax, e);
+        emin = skip ? emin : min(emin, e);
       }
+      int sigma = 0;
+      bool safe = true;
+      if (emax > -1000) {
+        sigma = 15 - emax;
+        safe = (emax <= 119) && (emin >= -141) && (emax - emin <= 32);
+      }
+      const int s1 = min(max(sigma, -126), 127), s2 = sigma - s1;  // 2^sigma as two exact factors
+      const float f1 = __uint_as_float((uint32_t)(127 + s1) << 23);
+      const float f2 = __uint_as_float((uint32_t)(127 + s2) << 23);
+#pragma unroll
+      for (int tc = 0; tc < 4; ++tc) {
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t two = wv[4 * tc + q];
+          float lo = __uint_as_float(two << 16), hi = __uint_as_float(two & 0xFFFF0000u);
+          if (safe) {
+            lo = __fmul_rn(__fmul_rn(lo, f1), f2);
+            hi = __fmul_rn(__fmul_rn(hi, f1), f2);
+          }
+          const __half2 h2 = __floats2half2_rn(lo, hi);
+          o[q] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
+        *reinterpret_cast<uint4*>(xs_s + xoff(r, g, tc, GB)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      float m = 0.0f;  // 0 marks the exact fallback
+      if (g >= G) m = 1.0f;
+      else if (safe) {
+        const int ns = -sigma;  // 2^-sigma, possibly subnormal (exact)
+        m = ns >= -126 ? __uint_as_float((uint32_t)(127 + ns) << 23) : __uint_as_float(0x00400000u >> (-127 - ns));
+      }
+      xm_s[r * gall + g] = m;
     }
   }
 }
