@@ -154,7 +154,9 @@ __device__ __noinline__ float chain_bf16_exact(uint4 codes, const uint16_t* xrow
 // other CTAs of the same launch) and are issued in batches so that many are in flight. Groups
 // from G up to the stage boundary are zero with multiplier 1, so that lanes past the end of the
 // reduction add +0 to their accumulators.
-template <int KIND, bool FROM_SMEM, bool SC_SMEM>
+// X32 (bf16 only): the rows are kept as fp32 values, unshifted (multiplier 1), in chunks of
+// 8 values at twice the f16 offsets; no group needs the exact fallback then.
+template <int KIND, bool FROM_SMEM, bool SC_SMEM, bool X32 = false>
 __device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const uint8_t* __restrict__ XS,
                            size_t sstride, int K, int G, int GB, uint8_t* xs_s, float* xm_s, const int* prow,
                            int real, int tid, int NT) {
@@ -226,6 +228,25 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const
                            : __ldcg(reinterpret_cast<const uint4*>(src + 16 * q));
       }
       const uint32_t* wv = reinterpret_cast<const uint32_t*>(v);
+      if (X32) {
+#pragma unroll
+        for (int tc = 0; tc < 4; ++tc) {
+          uint4 o0, o1;
+          o0.x = wv[4 * tc] << 16;
+          o0.y = wv[4 * tc] & 0xFFFF0000u;
+          o0.z = wv[4 * tc + 1] << 16;
+          o0.w = wv[4 * tc + 1] & 0xFFFF0000u;
+          o1.x = wv[4 * tc + 2] << 16;
+          o1.y = wv[4 * tc + 2] & 0xFFFF0000u;
+          o1.z = wv[4 * tc + 3] << 16;
+          o1.w = wv[4 * tc + 3] & 0xFFFF0000u;
+          uint4* dst = reinterpret_cast<uint4*>(xs_s + 2 * xoff(r, g, tc, GB));
+          dst[0] = o0;
+          dst[1] = o1;
+        }
+        xm_s[r * gall + g] = 1.0f;
+        continue;
+      }
       int emax = -1000, emin = 1000;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -412,7 +433,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
 // Consumers: consume the pass's S weight stages against activation buffer xs_s/xm_s, release
 // the buffer, then hand the eight-way-tree results of both columns of every real row to the
 // helper in epi[r][0..63] (column o at o, column 32 + o at 32 + o).
-template <int KIND, int T>
+template <int KIND, int T, bool X32 = false>
 __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, uint8_t* ring, const Bars& B,
                                          int bx, int be, uint32_t eph, bool ewait, volatile int* abort_flag,
                                          const uint8_t* xs_s, const float* xm_s, const int* prow,
@@ -429,7 +450,7 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
     acc0[r] = 0.0f;
     acc1[r] = 0.0f;
     xr[r] = min(r, real - 1);
-    xrow_s[r] = xs_s + xr[r] * GB * 512 + j * 16;
+    xrow_s[r] = xs_s + (X32 ? 2 : 1) * (xr[r] * GB * 512 + j * 16);
     xmrow_s[r] = xm_s + xr[r] * GB * 8 + j;
   }
   // ring position, advanced incrementally (no division per stage)
@@ -462,6 +483,34 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
         e2m1x8_to_f16x2(wB1[tc], b1[0], b1[1], b1[2], b1[3]);
 #pragma unroll
         for (int r = 0; r < T; ++r) {
+          if (X32) {
+            // fp32 rows: the same chunks at twice the offsets, plain fp32 fma (exact products)
+            const uint8_t* xp = xrow_s[r] + 2 * (s * 1024 + tc * 128);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {  // four values of each group at a time
+              const float4 xa = *reinterpret_cast<const float4*>(xp + 16 * hf);
+              const float4 xb = *reinterpret_cast<const float4*>(xp + 1024 + 16 * hf);
+#pragma unroll
+              for (int ii = 0; ii < 2; ++ii) {
+                const int i = 2 * hf + ii;
+                const float xa_lo = ii ? xa.z : xa.x, xa_hi = ii ? xa.w : xa.y;
+                const float xb_lo = ii ? xb.z : xb.x, xb_hi = ii ? xb.w : xb.y;
+                const __half2 wa0 = *reinterpret_cast<const __half2*>(&a0[i]);
+                const __half2 wa1 = *reinterpret_cast<const __half2*>(&a1[i]);
+                const __half2 wb0 = *reinterpret_cast<const __half2*>(&b0[i]);
+                const __half2 wb1 = *reinterpret_cast<const __half2*>(&b1[i]);
+                pA0[r] = __fmaf_rn(__low2float(wa0), xa_lo, pA0[r]);
+                pA0[r] = __fmaf_rn(__high2float(wa0), xa_hi, pA0[r]);
+                pA1[r] = __fmaf_rn(__low2float(wa1), xa_lo, pA1[r]);
+                pA1[r] = __fmaf_rn(__high2float(wa1), xa_hi, pA1[r]);
+                pB0[r] = __fmaf_rn(__low2float(wb0), xb_lo, pB0[r]);
+                pB0[r] = __fmaf_rn(__high2float(wb0), xb_hi, pB0[r]);
+                pB1[r] = __fmaf_rn(__low2float(wb1), xb_lo, pB1[r]);
+                pB1[r] = __fmaf_rn(__high2float(wb1), xb_hi, pB1[r]);
+              }
+            }
+            continue;
+          }
           // xoff(row, 16s + j (+ 8), tc) = row*GB*512 + s*1024 (+ 512) + tc*128 + j*16
           const uint8_t* xp = xrow_s[r] + s * 1024 + tc * 128;
           const uint4 xa = *reinterpret_cast<const uint4*>(xp);
@@ -488,14 +537,14 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
         } else {
           float qA0 = pA0[r], qA1 = pA1[r], qB0 = pB0[r], qB1 = pB1[r];
           const uint16_t* xrow = xraw + (size_t)prow[xr[r]] * pj.K;
-          if (mA == 0.0f) {
+          if (!X32 && mA == 0.0f) {
             qA0 = chain_bf16_exact(cA0, xrow, gA);
             qA1 = chain_bf16_exact(cA1, xrow, gA);
           } else {
             qA0 = __fmul_rn(qA0, mA);
             qA1 = __fmul_rn(qA1, mA);
           }
-          if (mB == 0.0f) {
+          if (!X32 && mB == 0.0f) {
             qB0 = chain_bf16_exact(cB0, xrow, gB);
             qB1 = chain_bf16_exact(cB1, xrow, gB);
           } else {
@@ -547,8 +596,9 @@ __device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const 
                                               volatile int* abort_flag, const uint8_t* xs_s, const float* xm_s,
                                               const int* prow, const uint16_t* xraw, int real, uint32_t& it,
                                               bool& dead, float* epi) {
-#define TFX_PASS(TT) \
-  run_pass<KIND, TT>(P, pj, ring, B, bx, be, eph, ewait, abort_flag, xs_s, xm_s, prow, xraw, real, it, dead, epi)
+#define TFX_PASS(TT)                                                                                  \
+  run_pass<KIND, TT, DOWN && KIND == TFX_ACT_BF16>(P, pj, ring, B, bx, be, eph, ewait, abort_flag, xs_s, xm_s, prow, \
+                                                   xraw, real, it, dead, epi)
   switch (t) {
     case 1: TFX_PASS(1); break;
     case 2: if constexpr (MAXR >= 2) TFX_PASS(2); break;
@@ -1018,13 +1068,20 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
           if (tsc)
             stage_rows<KIND, true, true>(raw, P.raw_row, raw + MAXR * P.raw_row, P.raw_sc, pj.K, pj.G, pj.GB, xs_s,
                                          xm_s, pd, q.real, lane, 32);
+          else if (KIND == TFX_ACT_BF16 && q.dn)
+            stage_rows<KIND, true, false, true>(raw, P.raw_row, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
+                                                lane, 32);
           else
             stage_rows<KIND, true, false>(raw, P.raw_row, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
                                           lane, 32);
         }
       } else if (!dead) {
-        stage_rows<KIND, false, false>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
-                                       lane, 32);
+        if (KIND == TFX_ACT_BF16 && q.dn)
+          stage_rows<KIND, false, false, true>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd,
+                                               q.real, lane, 32);
+        else
+          stage_rows<KIND, false, false>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.real,
+                                         lane, 32);
       }
       if (!pend_skip && !dead) {
         const int mine = lane < 8 ? row_of(q, lane) : 0;
@@ -1346,7 +1403,7 @@ extern "C" int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, cons
   P.h = const_cast<void*>(h);
   P.hs = const_cast<uint8_t*>(h_scale);
   P.out = out;
-  P.gbmax = P.pd.GB;
+  P.gbmax = (act_kind == TFX_ACT_BF16 ? 2 : 1) * P.pd.GB;  // bf16 h is staged as fp32
   set_raw(P, act_kind, P.pd.K, P.pd.G);
   P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * P.pd.units;
@@ -1391,7 +1448,7 @@ extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   P.y = y;
   P.y32 = y_f32_dbg;
   P.scratch = scratch;
-  P.gbmax = max(P.pu.GB, P.pd.GB);
+  P.gbmax = max(P.pu.GB, (act_kind == TFX_ACT_BF16 ? 2 : 1) * P.pd.GB);  // bf16 h is staged as fp32
   P.route_ints = 3 * d.n_experts + 2 + 3 * rows * d.top_k + rows + 2 * (NTHREADS / 32);
   set_raw(P, act_kind, max(P.pu.K, P.pd.K), max(P.pu.G, P.pd.G));
   P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
