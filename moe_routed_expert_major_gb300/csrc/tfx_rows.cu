@@ -247,15 +247,21 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const
         xm_s[r * gall + g] = 1.0f;
         continue;
       }
-      int emax = -1000, emin = 1000;
+      // the exponents of the largest and of the smallest nonzero finite magnitude (magnitude bits
+      // order like the values); NaN, Inf and zeros take no part
+      uint32_t mxb = 0u, mnb = 0xFFFFu;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const uint32_t bb = (wv[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-        const uint32_t ef = (bb >> 7) & 0xFFu, m = bb & 0x7Fu;
-        const bool skip = ef == 255u || (ef == 0u && m == 0u);  // NaN/Inf or zero
-        const int e = ef ? (int)ef - 127 : (31 - __clz((int)m)) - 133;
-        emax = skip ? emax : max(emax, e);
-        emin = skip ? emin : min(emin, e);
+        const uint32_t mag = (wv[j >> 1] >> (16 * (j & 1))) & 0x7FFFu;
+        const bool fin = mag - 1u < 0x7F7Fu;  // nonzero, exponent field below 255
+        mxb = max(mxb, fin ? mag : 0u);
+        mnb = min(mnb, fin ? mag : 0xFFFFu);
+      }
+      int emax = -1000, emin = 1000;
+      if (mxb) {
+        const uint32_t ex = mxb >> 7, en = mnb >> 7;
+        emax = ex ? (int)ex - 127 : (31 - __clz((int)(mxb & 0x7Fu))) - 133;
+        emin = en ? (int)en - 127 : (31 - __clz((int)(mnb & 0x7Fu))) - 133;
       }
       int sigma = 0;
       bool safe = true;
@@ -1012,16 +1018,18 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
     // whose buffer already holds its rows (every gate/up pass of a one-row launch, for one) is
     // not staged again.
     int krow0 = -1, krow1 = -1, kdn0 = -1, kdn1 = -1, kreal0 = 0, kreal1 = 0;
-    bool pend_skip = false;
-    auto same_rows = [&](const PassDesc& q) {
-      const bool b1 = NXB == 2 && (q.pidx & 1);
+    bool pend_skip = false, pend_copy = false;
+    // other: compare with the buffer the pass does not use (two buffers)
+    auto same_rows = [&](const PassDesc& q, bool other = false) {
+      const bool b1 = NXB == 2 && (((q.pidx & 1) != 0) != other);
       const int mine = lane < 8 ? row_of(q, lane) : 0;
       const bool eq = lane >= 8 || (b1 ? krow1 : krow0) == mine;
       return (b1 ? kdn1 : kdn0) == (int)q.dn && (b1 ? kreal1 : kreal0) == q.real && __all_sync(0xffffffffu, eq);
     };
     auto issue_raw = [&](const PassDesc& q) {
       pend_skip = same_rows(q);
-      if (pend_skip || !P.use_raw || dead) return;
+      pend_copy = !pend_skip && NXB == 2 && same_rows(q, true);  // the other buffer has them: copy it
+      if (pend_skip || pend_copy || !P.use_raw || dead) return;
       const Proj& pj = q.dn ? P.pd : P.pu;
       const int rowb = pj.K * AB;
       const bool tsc = KIND == TFX_ACT_E4M3 && (q.dn ? P.sc_tma_d : P.sc_tma_u);
@@ -1058,6 +1066,15 @@ __global__ void __launch_bounds__(NTHREADS, ((PH & PH_UPC) ? MAXR_U : MAXR_D) <=
       const uint8_t* XS = q.dn ? P.hs : P.xs;
       if (pend_skip) {
         // the buffer holds these rows already
+      } else if (pend_copy) {
+        if (!dead) {  // the other buffer holds these rows, staged the same way: copy its rows and multipliers
+          const int xb = (KIND == TFX_ACT_BF16 && q.dn ? 2 : 1) * q.real * pj.GB * 512;
+          const uint4* s4 = reinterpret_cast<const uint4*>(smem + Ly.xs + (bx ^ 1) * Ly.xs_stride);
+          uint4* d4 = reinterpret_cast<uint4*>(xs_s);
+          for (int i = lane; i < xb / 16; i += kWarp) d4[i] = s4[i];
+          const float* sm = reinterpret_cast<const float*>(smem + Ly.xm + (bx ^ 1) * Ly.xm_stride);
+          for (int i = lane; i < q.real * pj.GB * 8; i += kWarp) xm_s[i] = sm[i];
+        }
       } else if (P.use_raw) {
         if (raw_waited < raw_issued) {
           warp_wait(rawfull, raw_waited & 1u, P, abort_flag, dead);
