@@ -453,9 +453,9 @@ def run_ours(args):
         "roofline": {"kernel": kern_name, "bound": bound, "achieved": round(achieved, 1), "peak": hbm,
                      "peak_source": hbm_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                      "algorithmic_bytes_per_launch": int(kern_alg), "avg_launch_us": round(1000 * kern_avg_ms, 3),
-                     "traffic": (profiled_traffic("upc_chunk_%s_r%d" % (args.workload, R),
+                     "traffic": (profiled_traffic("upc_chunk_%s_%drow" % (args.workload, R),
                                                   ("tfx_chunk.cu", "tfx_common.cuh")) if chunk else
-                                 profiled_traffic("%s_rows_%s_r%d" % ("fused" if fused else "upc", args.workload, R))),
+                                 profiled_traffic("%s_rows_%s_%drow" % ("fused" if fused else "upc", args.workload, R))),
                      "tensor": tensor},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 5 if chunk else 4) * K, "clocks": clocks,
         "status": status, "launch": "cuda graph replay" if graph is not None else "eager",
