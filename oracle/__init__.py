@@ -152,6 +152,35 @@ def route(ids, E):
                 active=active[:na].copy(), n_active=na)
 
 
+def router(logits, k, mode=0, shared=-1):
+    """Routing ids and weights from router logits [R, n] (float64 arithmetic).
+
+    The pages take the routing as given; this follows the library's own routing convention
+    (the conventions of the synthetic inputs, which the rows kernels consume): the k largest
+    logits of a row, equal values going to the lower expert id, in descending order; NaN ranks
+    below every number (taken only when a row has fewer than k numbers), -0 equals +0.
+    mode 0: w_j = exp(l_j - l_0) / sum over the selected slots; mode 1: sigmoid scores
+    1 / (1 + exp(-l_j)) normalised to sum 1. shared >= 0 appends that expert id to every row
+    with weight 1. Returns (ids int32 [R, k (+1)], w float64 [R, k (+1)])."""
+    L = np.asarray(logits, np.float64)
+    R, n = L.shape
+    nan = np.isnan(L)
+    v = np.where(nan, 0.0, L)
+    idx = np.arange(n)
+    ids = np.zeros((R, k), np.int32)
+    w = np.zeros((R, k), np.float64)
+    for r in range(R):
+        order = np.lexsort((idx, -v[r], nan[r]))[:k]  # numbers first, then larger, then lower id
+        sel = L[r, order]
+        t = np.exp(sel - sel[0]) if mode == 0 else 1.0 / (1.0 + np.exp(-sel))
+        ids[r] = order
+        w[r] = t / t.sum()
+    if shared >= 0:
+        ids = np.concatenate([ids, np.full((R, 1), shared, np.int32)], axis=1)
+        w = np.concatenate([w, np.ones((R, 1))], axis=1)
+    return ids, w
+
+
 # ------------------------------------------------------------------ one output
 
 def chain_dot(wc, ws, xc, xs):
