@@ -344,6 +344,17 @@ def run_ours(args):
     torch.cuda.synchronize()
     breakdown = {n: 1000.0 * statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nb))
                  for j, n in enumerate(names)}
+    # the device router (top-k from logits) on logits of the same shape, for reference
+    lg = torch.randn((R, E), generator=torch.Generator().manual_seed(1), dtype=torch.float32).to(dev)
+    rids = torch.empty((R, k), dtype=torch.int32, device=dev)
+    rw = torch.empty((R, k), dtype=torch.float32, device=dev)
+    rev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+    for a, b in rev:
+        a.record(stream)
+        tfx.tfx_xp_router(lg, k, rids, rw)
+        b.record(stream)
+    torch.cuda.synchronize()
+    breakdown["router (logits -> ids, w; not in the step)"] = 1000.0 * statistics.median(a.elapsed_time(b) for a, b in rev)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None

@@ -196,6 +196,28 @@ int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t*
                       const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
                       const tfx_rows_opts* opts, void* stream);
 
+/* ---------------------------------------------------------------- router
+ * Routing ids and weights from router logits (no counterpart on the pages, which take the
+ * routing as given; this entry produces ids [R][k] and topk_w [R][k] in the form the entries
+ * above consume). For each row r of logits [rows][n_logits] (fp32, row-major, device):
+ *   selection: the top_k largest logits, ties going to the lower expert id; slot order is
+ *     descending logit (equal logits: lower id first). NaN ranks below every number and is
+ *     taken only when a row has fewer than top_k numbers; -0 and +0 are equal.
+ *   TFX_ROUTER_SOFTMAX: t_j = expf(l_j - l_0) (l_0 the largest selected logit),
+ *     s = t_0 + t_1 + ... + t_{k-1} summed in slot order in fp32, w_j = t_j / s.
+ *   TFX_ROUTER_SIGMOID: t_j = 1 / (1 + expf(-l_j)), then the same normalisation.
+ * shared_expert >= 0 appends a shared (always-routed) expert to every row: the rows of ids and
+ * topk_w then hold top_k + 1 slots, the last one shared_expert with weight 1. The layer is
+ * then called with top_k + 1 slots; shared_expert must index the packed weights and lie
+ * outside the routed ids (for example n_logits itself), or the route flags a duplicate.
+ * Limits: n_logits <= 1024, 1 <= top_k <= min(32, n_logits). rows = 0 is a no-op.
+ * Returns TFX_EINVAL for bad sizes, a bad mode or null pointers (rows > 0); TFX_ELAUNCH if
+ * the launch fails. One warp per row; asynchronous on `stream`. */
+#define TFX_ROUTER_SOFTMAX 0
+#define TFX_ROUTER_SIGMOID 1
+int tfx_xp_router(int32_t rows, int32_t n_logits, int32_t top_k, const float* logits, int32_t mode,
+                  int32_t shared_expert, int32_t* ids, float* topk_w, void* stream);
+
 /* ---------------------------------------------------------------- whole layer, one launch
  * Route, gate/up, down and combine of a small launch (R*k <= 256 routed pairs: decode) in a
  * single kernel launch, with the same results, bit for bit, as tfx_xp_route followed by

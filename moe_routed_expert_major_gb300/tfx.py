@@ -68,6 +68,7 @@ def load():
                                                _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_moe_rows_noalloc": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
+            "tfx_xp_router": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P]),
             "tfx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "tfx_version": (ctypes.c_int, []),
             "tfx_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
@@ -191,6 +192,17 @@ def tfx_xp_moe_rows_noalloc(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, 
                                           _ptr(rt["active"]), _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out),
                                           _ptr(y), _ptr(y_f32), _ptr(status), o, _stream()),
            "tfx_xp_moe_rows_noalloc")
+
+
+ROUTER_SOFTMAX = 0
+ROUTER_SIGMOID = 1
+
+
+def tfx_xp_router(logits, top_k, ids, topk_w, mode=ROUTER_SOFTMAX, shared_expert=-1):
+    """ids [R][k (+1)] int32 and topk_w [R][k (+1)] fp32 from logits [R][n] fp32 (device)."""
+    R, n = int(logits.shape[0]), int(logits.shape[1])
+    _check(load().tfx_xp_router(R, n, int(top_k), _ptr(logits), int(mode), int(shared_expert), _ptr(ids),
+                                _ptr(topk_w), _stream()), "tfx_xp_router")
 
 
 def tfx_selftest_wait_timeout(status, timeout_ns):

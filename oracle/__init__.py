@@ -172,9 +172,11 @@ def router(logits, k, mode=0, shared=-1):
     for r in range(R):
         order = np.lexsort((idx, -v[r], nan[r]))[:k]  # numbers first, then larger, then lower id
         sel = L[r, order]
-        t = np.exp(sel - sel[0]) if mode == 0 else 1.0 / (1.0 + np.exp(-sel))
+        with np.errstate(over="ignore", invalid="ignore"):  # -inf or NaN logits give 0, inf or NaN
+            t = np.exp(sel - sel[0]) if mode == 0 else 1.0 / (1.0 + np.exp(-sel))
         ids[r] = order
-        w[r] = t / t.sum()
+        with np.errstate(invalid="ignore"):
+            w[r] = t / t.sum()
     if shared >= 0:
         ids = np.concatenate([ids, np.full((R, 1), shared, np.int32)], axis=1)
         w = np.concatenate([w, np.ones((R, 1))], axis=1)
