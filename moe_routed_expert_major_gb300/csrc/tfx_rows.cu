@@ -424,6 +424,8 @@ struct Bars {
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const RowsParams& P,
                                           volatile int* abort_flag, bool& dead) {
   if (dead) return false;
+  // a completed phase needs neither the abort flag nor the bounded loop
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   bool ok = (*abort_flag == 0) && mbar_wait(bar, parity, P.timeout_ns);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) {
@@ -435,6 +437,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   }
   return ok;
 }
+
+// E8M0 code -> fp32 bits (those of e8m0_to_f32), a table read through L1 by the consumers.
+struct E8m0Table {
+  uint32_t v[256];
+  constexpr E8m0Table() : v() {
+    for (int c = 0; c < 256; ++c) v[c] = c == 0 ? 0x00400000u : c == 255 ? 0x7FC00000u : (uint32_t)c << 23;
+  }
+};
+__device__ const E8m0Table e8m0_table = E8m0Table();
+__device__ __forceinline__ float e8m0_lookup(uint32_t code) { return __uint_as_float(__ldg(e8m0_table.v + code)); }
 
 // Consumers: consume the pass's S weight stages against activation buffer xs_s/xm_s, release
 // the buffer, then hand the eight-way-tree results of both columns of every real row to the
@@ -470,8 +482,8 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, ui
       const uint4 cA1 = *reinterpret_cast<const uint4*>(tile + (32 + o) * CODE_B + 16 * j);
       const uint4 cB0 = *reinterpret_cast<const uint4*>(tile + o * CODE_B + 128 + 16 * j);
       const uint4 cB1 = *reinterpret_cast<const uint4*>(tile + (32 + o) * CODE_B + 128 + 16 * j);
-      const float sA0 = e8m0_to_f32(sc[o * GPS + j]), sA1 = e8m0_to_f32(sc[(32 + o) * GPS + j]);
-      const float sB0 = e8m0_to_f32(sc[o * GPS + 8 + j]), sB1 = e8m0_to_f32(sc[(32 + o) * GPS + 8 + j]);
+      const float sA0 = e8m0_lookup(sc[o * GPS + j]), sA1 = e8m0_lookup(sc[(32 + o) * GPS + j]);
+      const float sB0 = e8m0_lookup(sc[o * GPS + 8 + j]), sB1 = e8m0_lookup(sc[(32 + o) * GPS + 8 + j]);
       const int gA = s * GPS + j, gB = gA + 8;
       float pA0[T], pA1[T], pB0[T], pB1[T];
 #pragma unroll
