@@ -355,6 +355,15 @@ def run_ours(args):
         b.record(stream)
     torch.cuda.synchronize()
     breakdown["router (logits -> ids, w; not in the step)"] = 1000.0 * statistics.median(a.elapsed_time(b) for a, b in rev)
+    if E % 8 == 0 and E >= 16 and k <= 4 * (E // 8):  # group-limited sigmoid routing: 8 groups, 4 kept
+        rb = (0.1 * torch.randn(E, generator=torch.Generator().manual_seed(2), dtype=torch.float32)).to(dev)
+        for a, b in rev:
+            a.record(stream)
+            tfx.tfx_xp_router_grouped(lg, k, 8, 4, rids, rw, bias=rb, scale=2.5)
+            b.record(stream)
+        torch.cuda.synchronize()
+        breakdown["grouped router (8 groups, 4 kept; not in the step)"] = 1000.0 * statistics.median(
+            a.elapsed_time(b) for a, b in rev)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None

@@ -218,6 +218,28 @@ int tfx_xp_down_chunk(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t*
 int tfx_xp_router(int32_t rows, int32_t n_logits, int32_t top_k, const float* logits, int32_t mode,
                   int32_t shared_expert, int32_t* ids, float* topk_w, void* stream);
 
+/* Group-limited sigmoid routing (DeepSeek-V3 style; no counterpart on the pages either), in
+ * fp32 throughout, every step one IEEE operation rounded to nearest, so that ids and weights
+ * are fixed bit for bit by this definition. For each row of logits [rows][n_logits]:
+ *   s_e = sigmoid32(l_e): t = exp(max(-|l|, -86)) by Cody-Waite reduction (n = rint(y / ln 2),
+ *     r = (y - n*ln2_hi) - n*ln2_lo, ln2_hi with 16 significant bits) and the degree-7 Taylor
+ *     polynomial of exp(r) in Horner form, times 2^n; s = 1/(1+t) for l >= 0, t/(1+t) below.
+ *   c_e = s_e + bias[e] (bias [n_logits] fp32 on the device, or NULL: c_e = s_e).
+ *   The experts form n_group contiguous groups of n_logits / n_group; a group's score is the
+ *     fp32 sum of its two best c (best first). The topk_group best groups are kept (equal
+ *     scores: lower group first), and the top_k best experts of the kept groups by c are the
+ *     ids, best first (equal c: lower id first; NaN ranks below every number; -0 equals +0).
+ *   w_j = (s_j / S) * scale, S = s_0 + ... + s_{top_k-1} summed in slot order from +0. The
+ *     bias steers the choice only.
+ * shared_expert >= 0 appends a shared expert with weight 1, as for tfx_xp_router.
+ * Limits: n_logits <= 1024; 1 <= n_group <= 32 dividing n_logits into groups of at least 2;
+ * 1 <= topk_group <= n_group; 1 <= top_k <= min(32, topk_group * n_logits / n_group); scale not
+ * NaN. rows = 0 is a no-op. Returns TFX_EINVAL for bad sizes or null logits/ids/topk_w
+ * (rows > 0), TFX_ELAUNCH if the launch fails. One warp per row; asynchronous on `stream`. */
+int tfx_xp_router_grouped(int32_t rows, int32_t n_logits, int32_t top_k, const float* logits, const float* bias,
+                          int32_t n_group, int32_t topk_group, float scale, int32_t shared_expert, int32_t* ids,
+                          float* topk_w, void* stream);
+
 /* ---------------------------------------------------------------- whole layer, one launch
  * Route, gate/up, down and combine of a small launch (R*k <= 256 routed pairs: decode) in a
  * single kernel launch, with the same results, bit for bit, as tfx_xp_route followed by

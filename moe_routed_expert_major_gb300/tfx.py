@@ -69,6 +69,8 @@ def load():
             "tfx_xp_moe_rows_noalloc": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_router": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P]),
+            "tfx_xp_router_grouped": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _I32, _I32, ctypes.c_float, _I32,
+                                                     _P, _P, _P]),
             "tfx_strerror": (ctypes.c_char_p, [ctypes.c_int]),
             "tfx_version": (ctypes.c_int, []),
             "tfx_selftest_wait_timeout": (ctypes.c_int, [_P, ctypes.c_int64, _P]),
@@ -203,6 +205,15 @@ def tfx_xp_router(logits, top_k, ids, topk_w, mode=ROUTER_SOFTMAX, shared_expert
     R, n = int(logits.shape[0]), int(logits.shape[1])
     _check(load().tfx_xp_router(R, n, int(top_k), _ptr(logits), int(mode), int(shared_expert), _ptr(ids),
                                 _ptr(topk_w), _stream()), "tfx_xp_router")
+
+
+def tfx_xp_router_grouped(logits, top_k, n_group, topk_group, ids, topk_w, bias=None, scale=1.0, shared_expert=-1):
+    """Group-limited sigmoid routing: ids [R][k (+1)] int32 and topk_w [R][k (+1)] fp32 from
+    logits [R][n] fp32 and an optional bias [n] fp32 (device)."""
+    R, n = int(logits.shape[0]), int(logits.shape[1])
+    _check(load().tfx_xp_router_grouped(R, n, int(top_k), _ptr(logits), _ptr(bias),
+                                        int(n_group), int(topk_group), float(scale), int(shared_expert), _ptr(ids),
+                                        _ptr(topk_w), _stream()), "tfx_xp_router_grouped")
 
 
 def tfx_selftest_wait_timeout(status, timeout_ns):

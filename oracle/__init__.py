@@ -183,6 +183,85 @@ def router(logits, k, mode=0, shared=-1):
     return ids, w
 
 
+# fp32 constants of sigmoid32: 1/ln 2; ln 2 split after Cody and Waite into a 16-bit head
+# (n * head is exact for |n| < 128) and the rest; the Taylor coefficients 1/j! of exp.
+_F32 = np.float32
+_LOG2E = _F32(1.4426950408889634)
+_LN2_HI = _F32(0.693145751953125)
+_LN2_LO = _F32(0.6931471805599453 - 0.693145751953125)
+_INV_FACT = [_F32(1.0 / f) for f in (1, 1, 2, 6, 24, 120, 720, 5040)]
+
+
+def sigmoid32(l):
+    """The grouped router's sigmoid, every step one IEEE fp32 operation rounded to nearest.
+
+    t = exp(y) for y = max(-|l|, -86): n = rint(y / ln 2), r = (y - n*LN2_HI) - n*LN2_LO,
+    exp(r) by its degree-7 Taylor polynomial in Horner form (multiply, then add), times 2^n;
+    then 1 / (1 + t) for l >= 0 and t / (1 + t) for l < 0. NaN stays NaN. Logits below -86
+    are taken as -86 (their sigmoid is below 5e-38), so no step meets a subnormal."""
+    l = np.asarray(l, np.float32)
+    nan = np.isnan(l)
+    lz = np.where(nan, _F32(0.0), l)
+    y = np.maximum(-np.abs(lz), _F32(-86.0))
+    n = np.rint(y * _LOG2E)
+    r = (y - n * _LN2_HI) - n * _LN2_LO
+    p = np.full_like(r, _INV_FACT[7])
+    for c in _INV_FACT[6::-1]:
+        p = p * r + c
+    two_n = ((n.astype(np.int32) + 127) << 23).astype(np.int32).view(np.float32)
+    t = p * two_n
+    d = _F32(1.0) + t
+    s = np.where(lz >= 0, _F32(1.0) / d, t / d)
+    return np.where(nan, l, s).astype(np.float32)
+
+
+def _rank(v):
+    """Indices of v ordered by value, larger first, equal values by lower index, NaN last
+    (-0 equals +0)."""
+    v = np.asarray(v, np.float64)
+    nan = np.isnan(v)
+    return np.lexsort((np.arange(v.size), -np.where(nan, 0.0, v), nan))
+
+
+def router_grouped(logits, k, n_group, topk_group, bias=None, scale=1.0, shared=-1):
+    """Group-limited sigmoid routing (DeepSeek-V3 style), all arithmetic in fp32.
+
+    Per row: s = sigmoid32(l); choice scores c = s + bias (fp32 add; bias omitted: c = s). The
+    n experts form n_group contiguous groups of n / n_group; a group's score is the sum, in
+    fp32, of its two best choice scores (best first). The topk_group best groups are kept
+    (equal scores: lower group first); the k best experts of the kept groups by c are the ids,
+    in that order (equal scores: lower id first; NaN ranks below every number). Weights:
+    w_j = (s_j / S) * scale, S = s_0 + s_1 + ... summed in slot order in fp32 from +0. The
+    bias steers the choice only, never the weights. shared >= 0 appends that expert with
+    weight 1. Returns (ids int32 [R, k (+1)], w float32 [R, k (+1)])."""
+    L = np.asarray(logits, np.float32)
+    R, n = L.shape
+    gs = n // n_group
+    s = sigmoid32(L)
+    c = s + np.asarray(bias, np.float32)[None, :] if bias is not None else s
+    ids = np.zeros((R, k), np.int32)
+    w = np.zeros((R, k), np.float32)
+    for r in range(R):
+        G = np.zeros(n_group, np.float32)
+        for g in range(n_group):
+            grp = c[r, g * gs:(g + 1) * gs]
+            top = _rank(grp)[:2]
+            G[g] = _F32(grp[top[0]]) + _F32(grp[top[1]])
+        kept = _rank(G)[:topk_group]
+        allowed = np.concatenate([np.arange(g * gs, (g + 1) * gs) for g in sorted(kept)])
+        sel = allowed[_rank(c[r, allowed])[:k]]
+        ids[r] = sel
+        ssum = _F32(0.0)
+        for e in sel:
+            ssum = _F32(ssum + s[r, e])
+        with np.errstate(invalid="ignore"):
+            w[r] = (s[r, sel] / ssum) * _F32(scale)
+    if shared >= 0:
+        ids = np.concatenate([ids, np.full((R, 1), shared, np.int32)], axis=1)
+        w = np.concatenate([w, np.ones((R, 1), np.float32)], axis=1)
+    return ids, w
+
+
 # ------------------------------------------------------------------ one output
 
 def chain_dot(wc, ws, xc, xs):

@@ -103,3 +103,83 @@ def test_layer_routed_on_device_with_a_shared_expert(kind):
         assert gu.bits_equal(got["out"][r, j], c["d"][r, j])
     # y: the device's and the oracle's weights differ in the last bits: within the bound
     assert oracle.within_tol(got["y_f32"], f["y"], f["my"]).all()
+
+
+# ------------------------------------------------------------------ group-limited routing
+
+def run_grouped(L, k, ng, kg, bias=None, scale=1.0, shared=-1):
+    R = L.shape[0]
+    s = k + (1 if shared >= 0 else 0)
+    ld = torch.from_numpy(np.ascontiguousarray(L, np.float32)).to(gu.DEV)
+    bd = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias, np.float32)).to(gu.DEV)
+    ids = torch.full((R, s), -7, dtype=torch.int32, device=gu.DEV)
+    w = torch.full((R, s), -7.0, dtype=torch.float32, device=gu.DEV)
+    tfx.tfx_xp_router_grouped(ld, k, ng, kg, ids, w, bias=bd, scale=scale, shared_expert=shared)
+    torch.cuda.synchronize()
+    return ids.cpu().numpy(), w.cpu().numpy()
+
+
+def check_grouped(L, k, ng, kg, bias=None, scale=1.0, shared=-1):
+    ids, w = run_grouped(L, k, ng, kg, bias, scale, shared)
+    oid, ow = oracle.router_grouped(L, k, ng, kg, bias, scale, shared)
+    # every step is one IEEE fp32 operation on both sides: ids and weight bits are equal (a NaN
+    # weight, from NaN logits that had to be taken, is NaN on both sides; its payload may differ)
+    assert np.array_equal(ids, oid)
+    nan = np.isnan(ow)
+    assert np.array_equal(np.isnan(w), nan)
+    assert np.array_equal(w[~nan].view(np.uint32), ow[~nan].view(np.uint32))
+
+
+@pytest.mark.parametrize("shape", [(300, 256, 8, 4, 8), (5, 160, 8, 3, 6), (9, 1024, 32, 4, 32), (17, 64, 32, 32, 8),
+                                   (3, 2, 1, 1, 1)],
+                         ids=["deepseek", "ragged-groups", "wide", "pairs", "smallest"])
+def test_grouped_router_bit_equal_to_the_oracle(shape):
+    R, n, ng, kg, k = shape
+    rng = np.random.default_rng(R * 7 + n)
+    L = (rng.standard_normal((R, n)) * 3).astype(np.float32)
+    bias = (rng.standard_normal(n) * 0.1).astype(np.float32)
+    check_grouped(L, k, ng, kg, bias, 2.5)
+    check_grouped(L, k, ng, kg, None, 1.0)
+
+
+def test_grouped_router_golden_ties_nan_and_infinities():
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "router_grouped.json")) as f:
+        for c in json.load(f)["cases"]:
+            L = np.array([[float(v) for v in c["logits"]]], np.float32)
+            b = None if c["bias"] is None else np.array(c["bias"], np.float32)
+            ids, w = run_grouped(L, c["top_k"], c["n_group"], c["topk_group"], b, c["scale"])
+            assert ids[0].tolist() == c["ids"], c["name"]
+            assert w[0].view(np.uint32).tolist() == [int(v, 16) for v in c["w_bits"]], c["name"]
+    rng = np.random.default_rng(31)
+    L = (rng.integers(-2, 3, size=(40, 64)) * 0.5).astype(np.float32)  # many equal values
+    L[0, :] = 0.0
+    L[1, ::2] = -0.0
+    L[2, 5] = np.nan
+    L[2, 7] = np.inf
+    L[3, :] = np.nan
+    L[3, 10:14] = [1.0, -np.inf, 2.0, -0.0]
+    L[4, :] = -np.inf
+    L[5, :] = -200.0
+    bias = (rng.integers(-2, 3, size=64) * 0.25).astype(np.float32)
+    bias[9] = np.nan
+    check_grouped(L, 8, 8, 4, bias, 1.0)
+    check_grouped(L, 8, 8, 4, None, 2.5)
+
+
+def test_grouped_router_shared_slot_and_rejections():
+    L = np.random.default_rng(5).standard_normal((9, 256)).astype(np.float32)
+    check_grouped(L, 8, 8, 4, None, 2.5, shared=256)
+    ids, w = run_grouped(L, 8, 8, 4, None, 2.5, shared=256)
+    assert np.all(ids[:, 8] == 256) and np.all(w[:, 8] == 1.0)
+    lib = tfx.load()
+    x = torch.zeros(4, dtype=torch.float32, device=gu.DEV)
+    p = x.data_ptr()
+    # groups that do not divide n, groups of one, too many groups kept, k above the kept experts
+    assert lib.tfx_xp_router_grouped(1, 10, 2, p, None, 4, 1, 1.0, -1, p, p, None) == -1
+    assert lib.tfx_xp_router_grouped(1, 8, 2, p, None, 8, 1, 1.0, -1, p, p, None) == -1
+    assert lib.tfx_xp_router_grouped(1, 8, 2, p, None, 4, 5, 1.0, -1, p, p, None) == -1
+    assert lib.tfx_xp_router_grouped(1, 8, 5, p, None, 4, 2, 1.0, -1, p, p, None) == -1
+    assert lib.tfx_xp_router_grouped(1, 8, 2, None, None, 4, 2, 1.0, -1, p, p, None) == -1
+    assert lib.tfx_xp_router_grouped(0, 8, 2, None, None, 4, 2, 1.0, -1, None, None, None) == 0
