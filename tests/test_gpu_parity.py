@@ -112,6 +112,33 @@ def test_route_matches_oracle(orc):
         assert np.array_equal(rt["active"].cpu().numpy()[:ref["n_active"]], ref["active"])
 
 
+@pytest.mark.parametrize("shape", [(700, 3, 64), (1537, 8, 256), (1537, 8, 1024), (4096, 8, 256), (3001, 1, 8)],
+                         ids=["3-ctas", "13-ctas", "13-ctas-unstaged", "32-ctas", "ragged"])
+def test_route_in_several_ctas_matches_oracle(orc, shape):
+    # launches above 2,048 pairs split the scatter over CTAs (each counts every pair itself)
+    R, k, E = shape
+    rng = np.random.default_rng(R + E)
+    ids = np.stack([rng.permutation(E)[:k] for _ in range(R)]).astype(np.int32)
+    for _ in range(7):  # out-of-range ids and duplicates, spread over the blocks
+        ids[rng.integers(0, R), rng.integers(0, k)] = rng.choice([-1, E, 5 * E])
+        if k > 1:
+            r = rng.integers(0, R)
+            ids[r, -1] = ids[r, 0]
+    d = tfx.dims(64, 32, E, k)
+    rt = tfx.alloc_route(R, E, k, gu.DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=gu.DEV)
+    tfx.tfx_xp_route(d, R, torch.from_numpy(ids).to(gu.DEV), rt, st)
+    torch.cuda.synchronize()
+    ref = orc.route(ids, E)
+    n = int(ref["offs"][-1])
+    assert int(st.item()) == ref["status"]
+    assert np.array_equal(rt["offs"].cpu().numpy(), ref["offs"])
+    assert np.array_equal(rt["pair_row"].cpu().numpy()[:n], ref["pair_row"])
+    assert np.array_equal(rt["pair_slot"].cpu().numpy()[:n], ref["pair_slot"])
+    assert int(rt["n_active"].item()) == ref["n_active"]
+    assert np.array_equal(rt["active"].cpu().numpy()[:ref["n_active"]], ref["active"])
+
+
 def test_pack_layout(orc):
     """The packed stage layout, rebuilt here on the host from the canonical arrays."""
     lay = small_layer(synth.ACT_E4M3, H=1088, I=96, E=3, k=2, R=1, seed=4)
