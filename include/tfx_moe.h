@@ -126,7 +126,10 @@ int tfx_xp_pack(tfx_dims d, const uint8_t* wg, const uint8_t* sg, const uint8_t*
  * ids [R][k] (int32, row-major). Pairs of one expert are in ascending (row, slot) order;
  * active experts in ascending id. Invalid ids set TFX_ST_RANGE / TFX_ST_DUP in *status and
  * are left out. Output buffers: offs [E+1], pair_row and pair_slot [R*k],
- * active [min(R*k, E)], n_active [1]. E must be <= 1024. */
+ * active [min(R*k, E)], n_active [1]. E must be <= 1024. No scratch: launches of more than
+ * 2,048 pairs run one CTA per 1,024 pairs (at most one per SM), each of which counts every
+ * pair itself. Returns TFX_EINVAL for bad sizes or null pointers, TFX_ECUDA if the device
+ * query fails, TFX_ELAUNCH if the launch fails; asynchronous on `stream`. */
 int tfx_xp_route(tfx_dims d, int32_t rows, const int32_t* ids, int32_t* offs, int32_t* pair_row,
                  int32_t* pair_slot, int32_t* active, int32_t* n_active, int32_t* status, void* stream);
 
