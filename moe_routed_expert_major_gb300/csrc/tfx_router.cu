@@ -6,10 +6,9 @@
 // largest logits of a row are selected, ties going to the lower expert id, in descending
 // order; the weights are a softmax over the selected logits (or normalised sigmoid scores).
 //
-// One warp per row. Lane l holds logits l, l + 32, ... in registers; each of the k rounds
-// takes every lane's best remaining candidate, the warp's largest order key (redux.sync max)
-// and the lowest id holding it (redux.sync min); the winner lane retires it. Order keys rank
-// NaN below every number and -0 with +0, so that equal values go to the lower id.
+// One warp per row. Lane l holds logits l, l + 32, ... in registers and the k rounds of
+// topk_rounds pick the ids. Order keys rank NaN below every number and -0 with +0, so that
+// equal values go to the lower id.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -25,6 +24,31 @@ __device__ __forceinline__ uint32_t order_key(float v) {
   if (v != v) return 0u;
   uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// k rounds over the candidates this lane holds (bit i of live: candidate lane + 32 i, order
+// key key[i]); each round takes every lane's best remaining candidate (largest key, then
+// lower id), the warp's largest key (redux.sync max) and the lowest id holding it (redux.sync
+// min), and the winner lane retires it. Returns, in lane j < k, the id taken in round j.
+template <int NI>
+__device__ __forceinline__ int topk_rounds(const uint32_t (&key)[NI], uint32_t live, int k, int lane) {
+  int my_id = -1;
+  for (int j = 0; j < k; ++j) {
+    uint32_t bk = 0u;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
+      }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t cand = (bi >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
+    if (bi >= 0 && lane + 32 * bi == win) live &= ~(1u << bi);
+    if (lane == j) my_id = win;
+  }
+  return my_id;
 }
 
 template <int NI>
@@ -45,24 +69,7 @@ __global__ void __launch_bounds__(RO_WARPS * 32) router_kernel(const float* __re
 #pragma unroll
   for (int i = 0; i < NI; ++i)
     if (lane + 32 * i < E) live |= 1u << i;
-  int my_id = -1;  // lane j < k: the id selected in round j
-  for (int j = 0; j < k; ++j) {
-    // best candidate of this lane: largest key, then lowest id (lower i)
-    uint32_t bk = 0u;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < NI; ++i)
-      if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
-        bk = key[i];
-        bi = i;
-      }
-    // the warp's largest key, then the lowest id holding it
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
-    const uint32_t cand = (bi >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
-    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    if (bi >= 0 && lane + 32 * bi == win) live &= ~(1u << bi);
-    if (lane == j) my_id = win;
-  }
+  const int my_id = topk_rounds<NI>(key, live, k, lane);  // lane j < k: the id selected in round j
   // weights over the selected logits, in slot order
   float lv = 0.0f;
   if (lane < k) lv = __ldg(lrow + my_id);
@@ -175,22 +182,7 @@ __global__ void __launch_bounds__(RG_WARPS * 32)
     const int e = lane + 32 * i;
     if (e < E && ((gsel >> (e / gs)) & 1u)) live |= 1u << i;
   }
-  int my_id = -1;
-  for (int j = 0; j < k; ++j) {
-    uint32_t bk = 0u;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < NI; ++i)
-      if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
-        bk = key[i];
-        bi = i;
-      }
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
-    const uint32_t cand = (bi >= 0 && bk == kmax) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
-    const int win = (int)__reduce_min_sync(0xffffffffu, cand);
-    if (bi >= 0 && lane + 32 * bi == win) live &= ~(1u << bi);
-    if (lane == j) my_id = win;
-  }
+  const int my_id = topk_rounds<NI>(key, live, k, lane);
   // weights: the selected experts' sigmoid (no bias), normalised in slot order, then scaled
   const float sv = lane < k ? sigmoid32(__ldg(lrow + my_id)) : 0.0f;
   float ssum = 0.0f;
