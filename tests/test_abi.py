@@ -97,3 +97,27 @@ def test_chunk_entries_reject_before_launch(lib):
     assert L.tfx_xp_down_chunk(d, 4, 0, st, st, st, ctypes.byref(rt), None, st, None, None) == -1
     assert L.tfx_xp_down_chunk(d, 4, 1, st, st, st, ctypes.byref(rt), st, st, None, None) == -2
     assert L.tfx_xp_down_chunk(d, 0, 0, st, st, st, ctypes.byref(rt), st, st, None, None) == 0  # R = 0: no-op
+
+
+def test_router_entries_reject_before_launch(lib):
+    """Both routers check their sizes, mode and pointers before any launch; R = 0 is a no-op."""
+    L = lib
+    p = ctypes.c_void_p(64)  # never dereferenced: validation fails first
+    assert L.tfx_xp_router(1, 0, 1, p, 0, -1, p, p, None) == -1          # no logits
+    assert L.tfx_xp_router(1, 1025, 8, p, 0, -1, p, p, None) == -1       # more than 1,024 logits
+    assert L.tfx_xp_router(1, 256, 33, p, 0, -1, p, p, None) == -1       # top_k above 32
+    assert L.tfx_xp_router(1, 4, 5, p, 0, -1, p, p, None) == -1          # top_k above n_logits
+    assert L.tfx_xp_router(1, 256, 8, p, 2, -1, p, p, None) == -1        # unknown mode
+    assert L.tfx_xp_router(1, 256, 8, p, 0, -2, p, p, None) == -1        # bad shared expert
+    assert L.tfx_xp_router(1, 256, 8, None, 0, -1, p, p, None) == -1     # null logits
+    assert L.tfx_xp_router(0, 256, 8, None, 0, -1, None, None, None) == 0
+    g = lambda rows=1, n=256, k=8, lg=p, ng=8, kg=4, sc=1.0, sh=-1, ids=p, w=p: L.tfx_xp_router_grouped(
+        rows, n, k, lg, None, ng, kg, sc, sh, ids, w, None)
+    assert g(ng=0) == -1 and g(ng=33) == -1            # group count out of range
+    assert g(n=250) == -1                              # groups do not divide the experts
+    assert g(n=8, ng=8, kg=1, k=1) == -1               # groups of one expert
+    assert g(kg=0) == -1 and g(kg=9) == -1             # kept groups out of range
+    assert g(n=64, ng=8, kg=1, k=9) == -1              # top_k above the kept experts
+    assert g(sc=float("nan")) == -1                    # NaN scale
+    assert g(sh=-2) == -1 and g(lg=None) == -1 and g(w=None) == -1
+    assert g(rows=0, lg=None, ids=None, w=None) == 0
