@@ -30,7 +30,17 @@
  *   max 448). bf16: IEEE-754 binary32 with the low 16 bits dropped, rounded to nearest even.
  *
  * Compile with -ffp-contract=off so that every fp32 operation rounds where written.
+ *
+ * Planted controls: built with -DTFXO_CTL=n (n > 0), one deliberate mistake of a known kind
+ * is compiled in (the nibble order, the tree, the scale index, one accumulator for every
+ * group, the weight scale's bias, the chain's k order, the combine's slot order, the E4M3
+ * tie rule), so that a test can show
+ * that the pins catch it. TFXO_CTL 0, the default, is the oracle as it ships.
  */
+#ifndef TFXO_CTL
+#define TFXO_CTL 0
+#endif
+
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -93,7 +103,11 @@ int tfxo_e4m3_encode(double v) {
   frexp(a, &ex);
   ex -= 1;                              /* a in [2^ex, 2^(ex+1)) */
   int q = (ex < -6) ? -9 : ex - 3;      /* spacing of the E4M3 grid around a */
+#if TFXO_CTL == 8
+  double r = round(ldexp(a, -q));       /* planted: ties away from zero */
+#else
   double r = rint(ldexp(a, -q));        /* default rounding mode: nearest, ties to even */
+#endif
   double val = ldexp(r, q);
   if (val >= 448.0) return s | 0x7E;
   if (val < ldexp(1.0, -6)) return s | (int)(val * 512.0); /* subnormals: m * 2^-9 */
@@ -194,7 +208,11 @@ int tfxo_route(const int32_t* ids, int R, int k, int E, int32_t* offs, int32_t* 
 
 static int nibble(const uint8_t* codes, int k) {
   uint8_t b = codes[k >> 1];
+#if TFXO_CTL == 1
+  return (k & 1) ? (b & 15) : (b >> 4); /* planted: nibble order swapped */
+#else
   return (k & 1) ? (b >> 4) : (b & 15); /* the lower k sits in the low nibble */
+#endif
 }
 
 /* Unscaled element values of one activation row, and the fp32 value of each group's scale. */
@@ -225,14 +243,35 @@ float tfxo_chain_dot(int K, const uint8_t* wc, const uint8_t* ws, const float* x
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   for (int g = 0; g < K / 32; g++) {
     float p = 0.0f;
+#if TFXO_CTL == 6
+    for (int t = 31; t >= 0; t--) { /* planted: the chain runs from the last k down */
+      int k = 32 * g + t;
+      p = fmaf((float)tfxo_e2m1_value(nibble(wc, k)), xc[k], p);
+    }
+#else
     for (int t = 0; t < 32; t++) {
       int k = 32 * g + t;
       p = fmaf((float)tfxo_e2m1_value(nibble(wc, k)), xc[k], p);
     }
+#endif
+#if TFXO_CTL == 3
+    float s = ue8m0_f32(ws[0]) * xs[0]; /* planted: the first group's scale for the whole row */
+#elif TFXO_CTL == 5
+    float s = ldexpf(1.0f, (int)ws[g] - 128) * xs[g]; /* planted: E8M0 bias off by one */
+#else
     float s = ue8m0_f32(ws[g]) * xs[g];
+#endif
+#if TFXO_CTL == 4
+    acc[0] = fmaf(p, s, acc[0]); /* planted: every group into one accumulator */
+#else
     acc[g & 7] = fmaf(p, s, acc[g & 7]);
+#endif
   }
+#if TFXO_CTL == 2
+  return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])); /* planted: tree */
+#else
   return ((acc[0] + acc[4]) + (acc[2] + acc[6])) + ((acc[1] + acc[5]) + (acc[3] + acc[7]));
+#endif
 }
 
 /* float64 definition for one output, with its mass. */
@@ -319,7 +358,11 @@ void tfxo_combine_chain(int k, int H, const float* d /*[k][H]*/, const float* w 
                         uint16_t* y_bf16, float* y_f32) {
   for (int m = 0; m < H; m++) {
     float y = 0.0f;
+#if TFXO_CTL == 7
+    for (int j = k - 1; j >= 0; j--) y = fmaf(w[j], d[(size_t)j * H + m], y); /* planted: slots reversed */
+#else
     for (int j = 0; j < k; j++) y = fmaf(w[j], d[(size_t)j * H + m], y);
+#endif
     if (y_f32) y_f32[m] = y;
     y_bf16[m] = tfxo_f32_to_bf16(y);
   }
