@@ -48,3 +48,19 @@ def test_route_matches_sorted_triples(orc, seed):
     assert np.array_equal(got["offs"], offs)
     assert list(got["pair_row"]) == prow and list(got["pair_slot"]) == pslot
     assert list(got["active"]) == active and got["n_active"] == len(active)
+
+
+def test_route_ten_thousand_small_random_cases(orc):
+    # many small routings with out-of-range ids and repeats drawn freely (not only planted)
+    rng = np.random.default_rng(2024)
+    for _ in range(10000):
+        E = int(rng.integers(1, 17))
+        k = int(rng.integers(1, min(E, 4) + 1))
+        R = int(rng.integers(0, 13))
+        ids = rng.integers(-2, E + 2, size=(R, k)).astype(np.int32)
+        got = orc.route(ids, E)
+        st, offs, prow, pslot, active = _brute(ids, E)
+        assert got["status"] == st
+        assert np.array_equal(got["offs"], offs)
+        assert list(got["pair_row"]) == prow and list(got["pair_slot"]) == pslot
+        assert list(got["active"]) == active and got["n_active"] == len(active)
