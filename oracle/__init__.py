@@ -47,10 +47,12 @@ def lib():
                 "tfxo_ue8m0_value": (ctypes.c_double, [_I]),
                 "tfxo_bf16_to_f32": (ctypes.c_float, [ctypes.c_uint16]),
                 "tfxo_f32_to_bf16": (ctypes.c_uint16, [ctypes.c_float]),
+                "tfxo_f64_to_bf16": (ctypes.c_uint16, [ctypes.c_double]),
                 "tfxo_e4m3_encode": (_I, [ctypes.c_double]),
                 "tfxo_quant_e4m3_f32": (None, [_I, _P, _P, _P]),
                 "tfxo_quant_e4m3_f64": (None, [_I, _P, _P, _P]),
                 "tfxo_round_bf16": (None, [_I, _P, _P]),
+                "tfxo_round_bf16_f64": (None, [_I, _P, _P]),
                 "tfxo_route": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
                 "tfxo_chain_dot": (ctypes.c_float, [_I, _P, _P, _P, _P]),
                 "tfxo_f64_dot": (ctypes.c_double, [_I, _P, _P, _P, _P]),
@@ -106,6 +108,14 @@ def f32_to_bf16(a):
     a = np.ascontiguousarray(a, dtype=np.float32).ravel()
     out = np.empty(a.shape, dtype=np.uint16)
     lib().tfxo_round_bf16(a.size, _p(a), _p(out))
+    return out
+
+
+def f64_to_bf16(a):
+    """Each float64 rounded once, to nearest even, straight to bf16 bits (no binary32 step)."""
+    a = np.ascontiguousarray(a, dtype=np.float64).ravel()
+    out = np.empty(a.shape, dtype=np.uint16)
+    lib().tfxo_round_bf16_f64(a.size, _p(a), _p(out))
     return out
 
 
@@ -469,7 +479,7 @@ def layer_f64(layer, h_in=None, threads=None, rows=None):
         elif kind == ACT_E4M3:
             q, s = quant_e4m3_f64(hh)
         else:
-            q, s = f32_to_bf16(hh.astype(np.float32)), None
+            q, s = f64_to_bf16(hh), None  # h rounded once, from float64, to nearest even
         dd, md = down_f64(layer, e, q, s)
         return pr, gg, uu, hh, mg, mu, mh, dd, md
 

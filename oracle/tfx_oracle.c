@@ -34,7 +34,9 @@
  * Planted controls: built with -DTFXO_CTL=n (n > 0), one deliberate mistake of a known kind
  * is compiled in (the nibble order, the tree, the scale index, one accumulator for every
  * group, the weight scale's bias, the chain's k order, the combine's slot order, the E4M3
- * tie rule), so that a test can show
+ * tie rule, the mass as |sum| instead of sum of |terms|, the SwiGLU mass without its
+ * g (1 - s) derivative term, the combine mass with signed weights, bf16 rounding of a
+ * float64 through binary32), so that a test can show
  * that the pins catch it. TFXO_CTL 0, the default, is the oracle as it ships.
  */
 #ifndef TFXO_CTL
@@ -90,6 +92,31 @@ uint16_t tfxo_f32_to_bf16(float f) {
   uint32_t lsb = (u >> 16) & 1u;
   u += 0x7fffu + lsb;
   return (uint16_t)(u >> 16);
+}
+
+/* IEEE round-to-nearest-even from binary64 straight to bf16, one rounding (no binary32 step in
+ * between, which could round a value just past a bf16 midpoint onto it and then to even); values
+ * at or beyond the midpoint above the largest finite bf16 become infinity; NaN -> quiet NaN. */
+uint16_t tfxo_f64_to_bf16(double v) {
+  if (isnan(v)) return signbit(v) ? 0xFFC0u : 0x7FC0u;
+  uint16_t s = signbit(v) ? 0x8000u : 0u;
+  double a = fabs(v);
+  if (a == 0.0) return s;
+  if (isinf(a)) return s | 0x7F80u;
+#if TFXO_CTL == 12
+  return tfxo_f32_to_bf16((float)v); /* planted: rounded to binary32 first, then to bf16 */
+#else
+  int ex;
+  frexp(a, &ex);
+  ex -= 1;                              /* a in [2^ex, 2^(ex+1)) */
+  int q = (ex < -126) ? -133 : ex - 7;  /* spacing of the bf16 grid around a (8 significant bits) */
+  double val = ldexp(rint(ldexp(a, -q)), q);
+  if (val >= ldexp(1.0, 128)) return s | 0x7F80u;
+  float f = (float)val;                 /* exact: val lies on the bf16 grid */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return (uint16_t)(s | ((u >> 16) & 0x7FFFu));
+#endif
 }
 
 /* Nearest E4M3 code to v, ties to even, magnitudes beyond 448 saturated to 448; NaN -> 0x7F. */
@@ -163,6 +190,10 @@ void tfxo_quant_e4m3_f64(int n, const double* h, uint8_t* codes, uint8_t* scales
 
 void tfxo_round_bf16(int n, const float* h, uint16_t* out) {
   for (int i = 0; i < n; i++) out[i] = tfxo_f32_to_bf16(h[i]);
+}
+
+void tfxo_round_bf16_f64(int n, const double* h, uint16_t* out) {
+  for (int i = 0; i < n; i++) out[i] = tfxo_f64_to_bf16(h[i]);
 }
 
 /* ------------------------------------------------------------------ routing
@@ -283,6 +314,9 @@ double tfxo_f64_dot(int K, const uint8_t* wc, const uint8_t* ws, const double* x
     s += t;
     m += fabs(t);
   }
+#if TFXO_CTL == 9
+  m = fabs(s); /* planted: the mass taken as |sum of terms| instead of the sum of |terms| */
+#endif
   *mass = m;
   return s;
 }
@@ -331,7 +365,11 @@ void tfxo_silu_mul_f64(int n, const double* g, const double* u, const double* mg
   for (int i = 0; i < n; i++) {
     double s = 1.0 / (1.0 + exp(-g[i]));
     double si = g[i] * s;
+#if TFXO_CTL == 10
+    double d = s; /* planted: silu'(g) taken as the sigmoid alone, the g (1 - s) term dropped */
+#else
     double d = s * (1.0 + g[i] * (1.0 - s));
+#endif
     h[i] = si * u[i];
     mh[i] = fabs(d) * mg[i] * fabs(u[i]) + fabs(si) * mu[i] + fabs(h[i]);
   }
@@ -374,7 +412,11 @@ void tfxo_combine_f64(int k, int H, const double* d, const double* md, const flo
     double s = 0.0, ms = 0.0;
     for (int j = 0; j < k; j++) {
       s += (double)w[j] * d[(size_t)j * H + m];
+#if TFXO_CTL == 11
+      ms += (double)w[j] * md[(size_t)j * H + m]; /* planted: the weight's sign kept in the mass */
+#else
       ms += fabs((double)w[j]) * md[(size_t)j * H + m];
+#endif
     }
     y[m] = s;
     my[m] = ms;

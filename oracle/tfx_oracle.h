@@ -17,11 +17,13 @@ double tfxo_e4m3_value(int code);
 double tfxo_ue8m0_value(int code);
 float tfxo_bf16_to_f32(uint16_t b);
 uint16_t tfxo_f32_to_bf16(float f);
+uint16_t tfxo_f64_to_bf16(double v);
 int tfxo_e4m3_encode(double v);
 
 void tfxo_quant_e4m3_f32(int n, const float* h, uint8_t* codes, uint8_t* scales);
 void tfxo_quant_e4m3_f64(int n, const double* h, uint8_t* codes, uint8_t* scales);
 void tfxo_round_bf16(int n, const float* h, uint16_t* out);
+void tfxo_round_bf16_f64(int n, const double* h, uint16_t* out);
 
 int tfxo_route(const int32_t* ids, int R, int k, int E, int32_t* offs, int32_t* pair_row,
                int32_t* pair_slot, int32_t* active, int32_t* n_active);

@@ -46,6 +46,29 @@ def _dequant_x(lay):
     return x * np.exp2(np.repeat(lay["sx"].astype(np.float64) - 127, 32, axis=-1))
 
 
+def _bf16_value(b):
+    return float(np.array([int(b) << 16], np.uint32).view(np.float32)[0])
+
+
+def nearest_bf16(v):
+    """The bf16 value nearest to the float64 v, ties to the even code, found by search over the
+    codes next to binary32(v)'s truncation (an independent restatement of round-to-nearest)."""
+    if math.isnan(v) or math.isinf(v) or v == 0.0:
+        return v
+    if abs(v) >= 2.0 ** 128 - 2.0 ** 119:
+        return math.copysign(math.inf, v)
+    b0 = int(np.array([v], np.float32).view(np.uint32)[0] >> 16) & 0x7FFF
+    sign = 0x8000 if v < 0 else 0
+    best = None
+    for b in range(max(0, b0 - 2), min(0x7F7F, b0 + 2) + 1):
+        c = _bf16_value(sign | b)
+        key = (abs(v - c), b & 1)
+        if best is None or key < best[0]:
+            best = (key, c)
+    return best[1]
+
+
+
 @pytest.mark.parametrize("case", json.load(open(GOLDEN))["cases"], ids=lambda c: c["name"])
 def test_golden_chain_order(orc, case):
     K = case["K"]
@@ -130,8 +153,7 @@ def test_f64_matches_torch_float64_matmul(orc, kind):
             q, s = orc.quant_e4m3_f64(f["h"][r, j])
             hh = torch.from_numpy(q).view(torch.float8_e4m3fn).to(torch.float64).numpy() * np.exp2(np.repeat(s.astype(np.float64) - 127, 32))
         else:
-            q = orc.f32_to_bf16(f["h"][r, j].astype(np.float32))
-            hh = torch.from_numpy(q.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+            hh = np.array([nearest_bf16(v) for v in f["h"][r, j]])  # h rounded once from float64
         Wd = torch.from_numpy(_dequant_w(lay["wd"][e], lay["sd"][e]))
         d = (Wd @ torch.from_numpy(hh)).numpy()
         assert np.all(np.abs(f["d"][r, j] - d) <= 1e-12 * f["md"][r, j] + 1e-300)

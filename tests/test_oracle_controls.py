@@ -9,7 +9,7 @@ import sys
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-PINS = ["tests/test_oracle_chain.py", "tests/test_oracle_formats.py"]
+PINS = ["tests/test_oracle_chain.py", "tests/test_oracle_formats.py", "tests/test_oracle_mass.py"]
 
 CONTROLS = {
     1: "E2M1 nibble order swapped",
@@ -20,6 +20,10 @@ CONTROLS = {
     6: "the chain run from the last k down",
     7: "combine slots in reverse order",
     8: "E4M3 ties rounded away from zero",
+    9: "mass taken as the magnitude of the sum",
+    10: "SwiGLU mass without the g (1 - s) derivative term",
+    11: "combine mass with signed weights",
+    12: "bf16 of a float64 rounded through binary32",
 }
 
 
