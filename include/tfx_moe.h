@@ -149,9 +149,15 @@ int tfx_xp_upc_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* p
                     float* h_dbg, int32_t* status, const tfx_rows_opts* opts, void* stream);
 
 /* ---------------------------------------------------------------- down rows
+ * The down projection of the same page: the commit message of the rows kernels names
+ * tf_dsv41_xp_down_rows beside the gate/up kernel (passes sized by the rows left, padding
+ * rows computed and never written), and "What this changes" gives its products as fp4 by
+ * E4M3 (or bf16) in the same fp32 chain.
  * For every routed pair p: out[pair_row[p]][pair_slot[p]][0..H) = h[p] . Wd_e (fp32 chain).
  * h and h_scale as written by tfx_xp_upc_rows; out is fp32 [R][k][H]. Entries of pairs
- * that were left out (invalid ids) are not written. */
+ * that were left out (invalid ids) are not written. The expert's weights are read once per
+ * pass for all of the pass's pairs, as for gate/up. Returns TFX_EINVAL for bad sizes, kinds,
+ * null or misaligned pointers (h, packed 16-byte aligned) or a bad max_pass (1, 2 or 4). */
 int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* h,
                      const uint8_t* h_scale, const tfx_route* rt, float* out, int32_t* status,
                      const tfx_rows_opts* opts, void* stream);
@@ -280,11 +286,15 @@ int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* p
  * call. Arguments and results are those of tfx_xp_moe_rows without `scratch`; the caller
  * still passes every input and output buffer.
  * Limit: tfx_xp_moe_rows_scratch_bytes(d, R) <= 65536 bytes (16,384 counters), else
- * TFX_EUNSUPPORTED before anything is launched.
- * The first call on a device looks up the buffer's device address (cudaGetSymbolAddress);
- * make that first call before any stream capture on the device. Every call on a device
- * shares the one buffer: calls that overlap on the GPU (other streams, other threads) race
- * and give wrong results; serialise them. */
+ * TFX_EUNSUPPORTED. That size check comes first; then every other argument is checked as by
+ * tfx_xp_moe_rows, and only a call that passes them all clears the buffer and launches.
+ * The first call on a device looks up the buffer's device address (cudaGetSymbolAddress).
+ * With CUDA's default lazy module loading, that first use (or the first launch) also loads
+ * the library's module on the device, which allocates device memory (the buffer among it)
+ * and may synchronise: make one call at start-up, outside any stream capture and outside any
+ * region where allocation is not allowed, before relying on the no-allocation property.
+ * Every call on a device shares the one buffer: calls that overlap on the GPU (other streams,
+ * other threads) race and give wrong results; serialise them. */
 int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
                             const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
                             int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
@@ -292,9 +302,13 @@ int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const ui
                             const tfx_rows_opts* opts, void* stream);
 
 /* ---------------------------------------------------------------- combine
+ * The routing-weighted sum of a row's expert outputs, whose bf16 result "Receipt > Kernel
+ * contract" of the same page checks per row (the combine output, bit-equal alone or with
+ * other rows).
  * y[r][m] = fma chain over j = 0..k-1 of topk_w[r][j] * out[r][j][m] from +0, rounded to
  * bf16 (nearest even). out fp32 [R][k][H], topk_w fp32 [R][k], y bf16 bits [R][H],
- * y_f32_dbg fp32 [R][H] or NULL. */
+ * y_f32_dbg fp32 [R][H] or NULL. Returns TFX_EINVAL for bad dims, rows < 0 or null pointers
+ * (rows > 0). */
 int tfx_xp_combine(tfx_dims d, int32_t rows, const float* out, const float* topk_w, uint16_t* y,
                    float* y_f32_dbg, void* stream);
 

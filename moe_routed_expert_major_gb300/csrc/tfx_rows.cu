@@ -1446,20 +1446,26 @@ extern "C" size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows) {
   return sizeof(int32_t) * ((size_t)2 + 2 * (size_t)d.n_experts + (size_t)rows * (d.hidden / 64));  // see RowsParams
 }
 
-extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
-                               const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
-                               int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
-                               uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
-                               int32_t* status, const tfx_rows_opts* opts, void* stream) {
-  RowsParams P;
+namespace tfx {
+
+// Argument checks and parameters of the one-launch layer, without launching anything (shared
+// by tfx_xp_moe_rows and tfx_xp_moe_rows_noalloc, which checks every argument before it
+// touches its built-in counter buffer). `scratch` may be null here when check_scratch is 0.
+static int moe_rows_prepare(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                            const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
+                            int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
+                            uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
+                            bool check_scratch, int32_t* status, const tfx_rows_opts* opts, RowsParams& P, int& mu,
+                            int& md, int& max_items) {
   int rc = common_args(d, rows, act_kind, packed, x, x_scale, status, opts, P);
   if (rc) return rc;
   if ((int64_t)rows * d.top_k > FUSED_MAX_PAIRS) return TFX_EUNSUPPORTED;
-  const int mu = pass_of(opts, false, rows);
-  const int md = min(pass_of(opts, true, rows), 4);  // the down pass stops at 4 rows
+  mu = pass_of(opts, false, rows);
+  md = min(pass_of(opts, true, rows), 4);  // the down pass stops at 4 rows
   if (!((mu == 1 && md == 1) || (mu == 2 && md == 2) || (mu == 4 && md == 4) || (mu == 8 && md == 4)))
     return TFX_EINVAL;
-  if (!offs || !active || !n_active || !scratch || (reinterpret_cast<uintptr_t>(scratch) & 3u)) return TFX_EINVAL;
+  if (!offs || !active || !n_active) return TFX_EINVAL;
+  if (check_scratch && (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 3u))) return TFX_EINVAL;
   if (rows == 0) return TFX_OK;
   if (!ids || !topk_w || !pair_row || !pair_slot || !h || !aligned16(h) || !out || !y ||
       (act_kind == TFX_ACT_E4M3 && !h_scale))
@@ -1482,10 +1488,30 @@ extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   set_raw(P, act_kind, max(P.pu.K, P.pd.K), max(P.pu.G, P.pd.G));
   P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
   P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
-  const int max_items = min(rows * d.top_k, d.n_experts) * (P.pu.units + P.pd.units);
+  max_items = min(rows * d.top_k, d.n_experts) * (P.pu.units + P.pd.units);
+  return TFX_OK;
+}
+
+static int moe_rows_launch(const RowsParams& P, int32_t act_kind, int mu, int md, int max_items, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_FUSED>(P, mu, md, max_items, st);
   return dispatch<TFX_ACT_BF16, PH_FUSED>(P, mu, md, max_items, st);
+}
+
+}  // namespace tfx
+
+extern "C" int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
+                               const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
+                               int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
+                               uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
+                               int32_t* status, const tfx_rows_opts* opts, void* stream) {
+  RowsParams P;
+  int mu = 0, md = 0, max_items = 0;
+  const int rc = moe_rows_prepare(d, rows, act_kind, packed, x, x_scale, ids, topk_w, offs, pair_row, pair_slot,
+                                  active, n_active, h, h_scale, out, y, y_f32_dbg, scratch, true, status, opts, P,
+                                  mu, md, max_items);
+  if (rc || rows == 0) return rc;
+  return moe_rows_launch(P, act_kind, mu, md, max_items, stream);
 }
 
 // ------------------------------------------------------------------------------ no-alloc variant
@@ -1528,18 +1554,21 @@ extern "C" int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kin
                                        void* stream) {
   const size_t need = tfx_xp_moe_rows_scratch_bytes(d, rows) / sizeof(int32_t);
   if (need > (size_t)NOALLOC_SCRATCH_INTS) return TFX_EUNSUPPORTED;  // beyond the built-in buffer
+  // every other argument is checked before the built-in buffer is touched
+  RowsParams P;
+  int mu = 0, md = 0, max_items = 0;
+  int rc = moe_rows_prepare(d, rows, act_kind, packed, x, x_scale, ids, topk_w, offs, pair_row, pair_slot, active,
+                            n_active, h, h_scale, out, y, y_f32_dbg, nullptr, false, status, opts, P, mu, md,
+                            max_items);
+  if (rc || rows == 0) return rc;
   int32_t* scratch = nullptr;
-  if (need > 0 && rows > 0) {
-    const int rc = noalloc_scratch(&scratch);
-    if (rc) return rc;
-    // the counters must start at zero; a previous call on this device may have stopped early
-    if (cudaMemsetAsync(scratch, 0, need * sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return TFX_ELAUNCH;
-    }
-  } else {
-    scratch = reinterpret_cast<int32_t*>(16);  // never touched: zero rows or arguments rejected below
+  rc = noalloc_scratch(&scratch);
+  if (rc) return rc;
+  // the counters must start at zero; a previous call on this device may have stopped early
+  if (cudaMemsetAsync(scratch, 0, need * sizeof(int32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TFX_ELAUNCH;
   }
-  return tfx_xp_moe_rows(d, rows, act_kind, packed, x, x_scale, ids, topk_w, offs, pair_row, pair_slot, active,
-                         n_active, h, h_scale, out, y, y_f32_dbg, scratch, status, opts, stream);
+  P.scratch = scratch;
+  return moe_rows_launch(P, act_kind, mu, md, max_items, stream);
 }
