@@ -38,8 +38,11 @@ def expert_bytes(H, I):
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="repeat each timed region of --steps steps until the repeats total this much device time")
+    ap.add_argument("--no-sweep", action="store_true", help="time the named workload only")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode", choices=["tiny", "decode", "shared", "apart", "chunk"])
     ap.add_argument("--rows", type=int, default=None)
@@ -167,6 +170,218 @@ class Clocks:
 
 # ------------------------------------------------------------------------------------ ours
 
+# Configurations of the metric beside the headline (decode, 1 row): rows on the same 8 experts
+# (E4M3), rows routed apart (bf16), and the 4,096-row prompt chunk on the tensor cores.
+SWEEP = ([("shared", R, "e4m3", "fused") for R in (2, 3, 4, 5, 8, 16)] +
+         [("apart", R, "bf16", "fused") for R in (2, 4, 8, 16)] + [("chunk", 4096, "e4m3", "chunk")])
+
+
+def fma_peak(sms, mhz):
+    """fp32-chain multiply-adds per second: SMs x 128 fma lanes per clock x the SM clock."""
+    return sms * 128 * mhz * 1e6
+
+
+class Runner:
+    """One workload on the device: inputs resident in HBM, the step (one whole layer), CUDA
+    graphs of its steps, and the timed repeats."""
+
+    def __init__(self, ctx, workload, R, act, path):
+        import numpy as np
+        import torch
+
+        import synth
+        from moe_routed_expert_major_gb300 import tfx
+        self.ctx = ctx
+        tfx_ = tfx
+        over = {"R": R}
+        if act is not None:
+            over["kind"] = synth.ACT_E4M3 if act == "e4m3" else synth.ACT_BF16
+        if ctx["E_over"] is not None:
+            over["E"] = ctx["E_over"]
+        cfg = synth.workload(workload, **over)
+        self.cfg = cfg
+        H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
+        dev = ctx["dev"]
+        self.d = tfx_.dims(H, I, E, k)
+        self.inp = inp = synth.make_inputs(cfg)
+        if kind == synth.ACT_E4M3:
+            self.x = torch.from_numpy(inp["x"]).to(dev)
+            self.xs = torch.from_numpy(inp["sx"]).to(dev)
+        else:
+            self.x = torch.from_numpy(inp["x"].view(np.int16)).to(dev)
+            self.xs = None
+        self.ids = torch.from_numpy(inp["ids"]).to(dev)
+        self.w = torch.from_numpy(inp["w"]).to(dev)
+        self.path = path
+        self.chunk = path == "chunk"
+        self.fused = path == "fused" and R * k <= 256
+        self.buf = tfx_.alloc_layer(R, H, I, E, k, kind, dev, chunk=self.chunk)
+        self.n_distinct = len(set(int(e) for e in inp["ids"].ravel()))
+        self.wbytes = self.n_distinct * expert_bytes(H, I)
+        P = R * k
+        act_b = 1 if kind == synth.ACT_E4M3 else 2
+        x_b = R * H * act_b + (R * (H // 32) if kind == synth.ACT_E4M3 else 0)
+        h_b = P * I * act_b + (P * (I // 32) if kind == synth.ACT_E4M3 else 0)
+        # algorithmic bytes of one layer: the distinct experts' weights once, activations in, h
+        # written and read back, the expert outputs written and read back by the combine,
+        # ids/weights, and y
+        self.alg_bytes = self.wbytes + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
+        self.fmas = P * 3 * H * I       # multiply-adds of the fp32 chains (one per weight per routed pair)
+        self.flops = 2.0 * self.fmas    # the same as flops, for the tensor-core path
+        self.launches = 1 if self.fused else (5 if self.chunk else 4)
+        self.tfx = tfx_
+
+    def step(self, i, ev=None, st=None):
+        tfx, d, R, kind, buf = self.tfx, self.d, self.cfg["R"], self.cfg["kind"], self.buf
+        pk = self.ctx["packed"][i % len(self.ctx["packed"])]
+        x, xs, ids, w = self.x, self.xs, self.ids, self.w
+        if self.fused:
+            if ev is not None:
+                ev[0].record(st)
+            tfx.tfx_xp_moe_rows(d, R, kind, pk, x, xs, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
+                                buf["y"], buf["scratch"], buf["status"])
+            if ev is not None:
+                ev[1].record(st)
+            return
+        tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
+        if ev is not None:
+            ev[0].record(st)
+        if self.chunk:
+            tfx.tfx_xp_upc_chunk(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
+                                 buf["status"])
+        else:
+            tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+        if ev is not None:
+            ev[1].record(st)
+        if self.chunk:
+            tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        else:
+            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
+        tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
+
+    def warm(self, W):
+        import torch
+        for i in range(max(3, W)):
+            self.step(i)
+        torch.cuda.synchronize()
+        st = int(self.buf["status"].item())
+        if st != 0:
+            raise RuntimeError("device status %d during warm-up (%s)" % (st, self.cfg["name"]))
+
+    def capture(self, n, events=None):
+        """A CUDA graph of steps 0..n-1 (cycling over the layer copies), or None."""
+        import torch
+        if n <= 0:
+            return None
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream()
+        cs.wait_stream(self.ctx["stream"])
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for i in range(n):
+                    self.step(i, None if events is None else events[i], torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return g
+
+    def timed(self, K, min_total_s, world, eager=False, clock_index=0):
+        """Exactly K steps per timed region, the region repeated (barrier and synchronisation on
+        both sides of each) until the repeats add up to min_total_s of device time; returns the
+        median repeat and the clock record of the whole loop."""
+        import torch
+        G = 8 * len(self.ctx["packed"])
+        graph = rem = None
+        if not eager:
+            try:
+                graph = self.capture(min(G, K))
+                rem = self.capture(K % min(G, K)) if K > G else None
+                for _ in range(2):
+                    graph.replay()
+                    if rem is not None:
+                        rem.replay()
+                torch.cuda.synchronize()
+            except (TypeError, RuntimeError) as ex:
+                sys.stderr.write("graph capture unavailable (%s); timing eager launches\n" % ex)
+                graph = rem = None
+        full = K // min(G, K) if graph is not None else 0
+        stream = self.ctx["stream"]
+        clk = Clocks(clock_index)
+        clk.start()
+        time.sleep(0.25)
+        times = []
+        total = 0.0
+        while (total < 1000.0 * min_total_s or len(times) < 3) and len(times) < 100000:
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            if graph is not None:
+                for _ in range(full):
+                    graph.replay()
+                if rem is not None:
+                    rem.replay()
+            else:
+                for i in range(K):
+                    self.step(i)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            ms = t0.elapsed_time(t1)
+            times.append(ms)
+            total += ms
+        clocks = clk.stop()
+        med = statistics.median(times)
+        return {"ms": med, "repeats": len(times), "clocks": clocks,
+                "launch": ("cuda graph replay: %d x a %d-step graph%s" % (full, min(G, K), (
+                    " + a %d-step graph" % (K % min(G, K))) if rem is not None else "")) if graph is not None
+                else "eager"}
+
+    def kernel_ms(self, K):
+        """Average duration of the roofline kernel (the fused launch, or gate/up) by CUDA
+        events captured around it in a graph of the same steps, replayed after the timed region."""
+        import torch
+        G = min(8 * len(self.ctx["packed"]), K)
+        kev = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
+        try:
+            g = self.capture(G, kev)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            return statistics.fmean(a.elapsed_time(b) for a, b in kev), "events around the kernel in a graph replay"
+        except (TypeError, RuntimeError):
+            kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+            for i in range(G):
+                self.step(i, kev[i], self.ctx["stream"])
+            torch.cuda.synchronize()
+            return statistics.fmean(a.elapsed_time(b) for a, b in kev), "events around eager launches"
+
+
+def bound_of(run, us, hbm, sm_mhz, sms):
+    """The binding roofline of one measured layer: HBM on its algorithmic bytes, the fp32-chain
+    fma rate (rows path), or the tensor cores (chunk path), whichever takes longest."""
+    t_hbm = run.alg_bytes / (hbm * 1e9)
+    out = {"hbm_us": round(1e6 * t_hbm, 2), "hbm_frac": round(1e6 * t_hbm / us, 4)}
+    if run.chunk:
+        tpeak, tsrc = tensor_peak_fp8()
+        t_t = run.flops / (tpeak * 1e12)
+        out.update({"tensor_us": round(1e6 * t_t, 2), "tensor_peak_tflops": tpeak, "tensor_peak_source": tsrc,
+                    "tensor_frac": round(1e6 * t_t / us, 4)})
+        bound, t = ("tensor", t_t) if t_t > t_hbm else ("hbm", t_hbm)
+    else:
+        fpk = fma_peak(sms, sm_mhz)
+        t_a = run.fmas / fpk
+        out.update({"alu_us": round(1e6 * t_a, 2), "alu_frac": round(1e6 * t_a / us, 4),
+                    "alu_peak": "%d SMs x 128 fp32 fma/clk x %.0f MHz (median SM clock sampled under load) = %.1f T fma/s"
+                                % (sms, sm_mhz, fpk / 1e12)})
+        bound, t = ("alu", t_a) if t_a > t_hbm else ("hbm", t_hbm)
+    out["bound"] = bound
+    out["frac"] = round(1e6 * t / us, 4)
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -183,163 +398,68 @@ def run_ours(args):
     dev = "cuda:%d" % local
     _build.build()
     tfx.load()
+    sms = torch.cuda.get_device_properties(local).multi_processor_count
 
-    over = {} if args.rows is None else {"R": args.rows}
-    if args.experts is not None:
-        over["E"] = args.experts
-    if args.act is not None:
-        over["kind"] = synth.ACT_E4M3 if args.act == "e4m3" else synth.ACT_BF16
-    cfg = synth.workload(args.workload, **over)
-    H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
-    d = tfx.dims(H, I, E, k)
-    inp = synth.make_inputs(cfg)
-    if kind == synth.ACT_E4M3:
-        x = torch.from_numpy(inp["x"]).to(dev)
-        xs = torch.from_numpy(inp["sx"]).to(dev)
-    else:
-        x = torch.from_numpy(inp["x"].view(np.int16)).to(dev)
-        xs = None
-    ids = torch.from_numpy(inp["ids"]).to(dev)
-    w = torch.from_numpy(inp["w"]).to(dev)
+    # packed weight copies, shared by every workload (same widths): each step uses the next one
+    E = args.experts if args.experts is not None else synth.WORKLOADS["decode"]["E"]
+    H, I = synth.WORKLOADS["decode"]["H"], synth.WORKLOADS["decode"]["I"]
     L = max(1, args.layers)
+    d0 = tfx.dims(H, I, E, synth.WORKLOADS["decode"]["k"])
     packed = []
     for l in range(L):
-        dw = synth.weights_torch(E, H, I, cfg["seed"] + 7919 * l, dev)
-        p = torch.empty(tfx.tfx_xp_packed_bytes(d), dtype=torch.uint8, device=dev)
-        tfx.tfx_xp_pack(d, dw, p)
+        dw = synth.weights_torch(E, H, I, synth.workload(args.workload)["seed"] + 7919 * l, dev)
+        p = torch.empty(tfx.tfx_xp_packed_bytes(d0), dtype=torch.uint8, device=dev)
+        tfx.tfx_xp_pack(d0, dw, p)
         packed.append(p)
         del dw
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
+    ctx = {"dev": dev, "packed": packed, "stream": torch.cuda.current_stream(), "E_over": args.experts}
+
     path = args.path or ("chunk" if args.workload == "chunk" else "fused")
-    chunk = path == "chunk"
-    buf = tfx.alloc_layer(R, H, I, E, k, kind, dev, chunk=chunk)
-    n_distinct = len(set(int(e) for e in inp["ids"].ravel()))
-    wbytes = n_distinct * expert_bytes(H, I)
-    stream = torch.cuda.current_stream()
-
-    fused = path == "fused" and R * k <= 256
-
-    def step(i, ev=None, st=None):
-        pk = packed[i % L]
-        st = stream if st is None else st
-        if fused:
-            if ev is not None:
-                ev[0].record(st)
-            tfx.tfx_xp_moe_rows(d, R, kind, pk, x, xs, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
-                                buf["y"], buf["scratch"], buf["status"])
-            if ev is not None:
-                ev[1].record(st)
-            return
-        tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
-        if ev is not None:
-            ev[0].record(st)
-        if chunk:
-            tfx.tfx_xp_upc_chunk(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
-                                 buf["status"])
-        else:
-            tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
-        if ev is not None:
-            ev[1].record(st)
-        if chunk:
-            tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
-        else:
-            tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
-        tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
-
-    for i in range(max(3, args.warmup)):
-        step(i)
-    torch.cuda.synchronize()
-    if int(buf["status"].item()) != 0:
-        raise RuntimeError("device status %d during warm-up" % int(buf["status"].item()))
+    main = Runner(ctx, args.workload, args.rows if args.rows is not None else synth.WORKLOADS[args.workload]["R"],
+                  args.act, path)
+    cfg = main.cfg
+    H, I, E, k, R, kind = cfg["H"], cfg["I"], cfg["E"], cfg["k"], cfg["R"], cfg["kind"]
+    d = main.d
+    K = max(1, args.steps)
+    main.warm(args.warmup)
 
     # ---------------------------------------------------------------- timed region
-    # Steps are replayed from a CUDA graph (G steps cycling over the layer copies), so the
-    # host's launch rate does not shape the device timeline; --eager launches every step from
-    # Python instead. A second graph of the same steps brackets the roofline kernel of every
-    # step with timing events; it is replayed right after the timed region for the kernel's
-    # launch duration, so that the event nodes do not slow the throughput measurement.
-    K = args.steps
-    G = 8 * L
-    graph = graph_ev = None
-    kev = [(torch.cuda.Event(enable_timing=True, external=True),
-            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(G)]
-    if not args.eager:
-        try:
-            graph = torch.cuda.CUDAGraph()
-            graph_ev = torch.cuda.CUDAGraph()
-            cs = torch.cuda.Stream()
-            cs.wait_stream(stream)
-            with torch.cuda.stream(cs):
-                with torch.cuda.graph(graph, stream=cs):
-                    for i in range(G):
-                        step(i, None, torch.cuda.current_stream())
-                with torch.cuda.graph(graph_ev, stream=cs):
-                    for i in range(G):
-                        step(i, kev[i], torch.cuda.current_stream())
-            torch.cuda.synchronize()
-            for _ in range(2):
-                graph.replay()
-                graph_ev.replay()
-            torch.cuda.synchronize()
-        except (TypeError, RuntimeError) as ex:  # no graph timing events in this torch: eager
-            sys.stderr.write("graph capture unavailable (%s); timing eager launches\n" % ex)
-            graph = graph_ev = None
-    if graph is not None:
-        K = max(G, (K + G - 1) // G * G)
-    else:
-        kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    clk = Clocks(local)
-    clk.start()
-    time.sleep(0.25)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0.record(stream)
-    if graph is not None:
-        for _ in range(K // G):
-            graph.replay()
-    else:
-        for i in range(K):
-            step(i, kev[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = clk.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if graph_ev is not None:  # the roofline kernel's launch durations (last replay's G launches)
-        for _ in range(max(2, min(16, K // G))):
-            graph_ev.replay()
-        torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
-    elapsed_ms = max_over_ranks(elapsed_ms, world)
-    status = int(buf["status"].item())
+    tm = main.timed(K, args.min_seconds, world, eager=args.eager, clock_index=local)
+    elapsed_ms = max_over_ranks(tm["ms"], world)
+    clocks = tm["clocks"]
+    status = int(main.buf["status"].item())
+    kern_ms, kern_how = main.kernel_ms(K)
+    if main.fused and not args.eager:
+        # one launch per step: the step time bounds the launch's duration from above, and the
+        # event brackets of the replay add their own delay
+        kern_ms = min(kern_ms, elapsed_ms / K)
 
-    # per-kernel breakdown (diagnostic, outside the timed region)
-    names = ["route", "upc_chunk", "down_chunk", "combine"] if chunk else ["route", "upc_rows", "down_rows", "combine"]
-    nb = min(200, K)
+    # per-kernel breakdown of the separate launches (diagnostic, outside the timed region)
+    names = ["route", "upc_chunk", "down_chunk", "combine"] if main.chunk else ["route", "upc_rows", "down_rows",
+                                                                               "combine"]
+    buf, stream = main.buf, ctx["stream"]
+    nb = 200
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(nb)]
     for i in range(nb):
         pk = packed[i % L]
         e = evs[i]
         e[0].record(stream)
-        tfx.tfx_xp_route(d, R, ids, buf["route"], buf["status"])
+        tfx.tfx_xp_route(d, R, main.ids, buf["route"], buf["status"])
         e[1].record(stream)
-        if chunk:
-            tfx.tfx_xp_upc_chunk(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
-                                 buf["status"])
+        if main.chunk:
+            tfx.tfx_xp_upc_chunk(d, R, kind, pk, main.x, main.xs, buf["route"], buf["h"], buf["h_scale"],
+                                 buf["chunk_ws"], buf["status"])
         else:
-            tfx.tfx_xp_upc_rows(d, R, kind, pk, x, xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
+            tfx.tfx_xp_upc_rows(d, R, kind, pk, main.x, main.xs, buf["route"], buf["h"], buf["h_scale"], buf["status"])
         e[2].record(stream)
-        if chunk:
+        if main.chunk:
             tfx.tfx_xp_down_chunk(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
         else:
             tfx.tfx_xp_down_rows(d, R, kind, pk, buf["h"], buf["h_scale"], buf["route"], buf["out"], buf["status"])
         e[3].record(stream)
-        tfx.tfx_xp_combine(d, R, buf["out"], w, buf["y"])
+        tfx.tfx_xp_combine(d, R, buf["out"], main.w, buf["y"])
         e[4].record(stream)
     torch.cuda.synchronize()
     breakdown = {n: 1000.0 * statistics.median(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(nb))
@@ -368,6 +488,7 @@ def run_ours(args):
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
     if not args.no_e2e:
+        inp = main.inp
         # the step's inputs travel in one copy: x, its scales, ids and weights packed into one
         # pinned host buffer (256-byte aligned parts) and read on the device through views
         parts = [("x", np.ascontiguousarray(inp["x"] if kind == synth.ACT_E4M3 else inp["x"].view(np.int16))),
@@ -393,15 +514,15 @@ def run_ours(args):
         hy = torch.empty(buf["y"].shape, dtype=buf["y"].dtype).pin_memory()
         h2d = tot
         d2h = hy.numel() * hy.element_size()
-        Ke = min(K, 2000) if not chunk else min(K, 20)
+        Ke = max(K, min(2000, int(0.5e6 / max(1.0, 1000.0 * elapsed_ms / K)))) if not main.chunk else min(K, 20)
 
         def e2e_step(i):
             din.copy_(hin, non_blocking=True)
             pk = packed[i % L]
-            if fused:
+            if main.fused:
                 tfx.tfx_xp_moe_rows(d, R, kind, pk, dx, dxs, dids, dwt, buf["route"], buf["h"], buf["h_scale"],
                                     buf["out"], buf["y"], buf["scratch"], buf["status"])
-            elif chunk:
+            elif main.chunk:
                 tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
                 tfx.tfx_xp_upc_chunk(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
                                      buf["status"])
@@ -424,79 +545,103 @@ def run_ours(args):
             e2e_step(i)
         b.record(stream)
         torch.cuda.synchronize()
-        e2e = {"value": 1000.0 * a.elapsed_time(b) / Ke, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": Ke}
+        e2e = {"value": round(1000.0 * a.elapsed_time(b) / Ke, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": Ke,
+               "how": "the public API (ctypes binding of libtfx_moe.so) launched from Python each step: one pinned "
+                      "H2D copy of the step's inputs, the layer, one D2H copy of y, back to back on one stream"}
+
+    # ---------------------------------------------------------------- the rest of the metric
+    hbm, hbm_src = peaks()
+    sm_mhz = clocks.get("sm_mhz") or 2070.0
+    sweep = []
+    if not args.no_sweep:
+        for wl, Rs, act, pth in SWEEP:
+            if (wl, Rs) == (args.workload, R):
+                continue
+            try:
+                run = Runner(ctx, wl, Rs, act, pth)
+                run.warm(args.warmup)
+                t = run.timed(K, args.min_seconds, world, eager=args.eager, clock_index=local)
+                ms = max_over_ranks(t["ms"], world)
+                us = 1000.0 * ms / K
+                mhz = t["clocks"].get("sm_mhz") or sm_mhz
+                ent = {"workload": wl, "rows": Rs, "act": act, "path": "fused one-launch layer" if run.fused else (
+                    "route + gate/up chunk + down chunk (tensor cores) + combine" if run.chunk else "four launches"),
+                       "distinct_experts": run.n_distinct, "us_per_layer": round(us, 3),
+                       "weight_gbs": round(run.wbytes / (us * 1e-6) / 1e9, 1),
+                       "weight_gbs_frac_of_peak": round(run.wbytes / (us * 1e-6) / 1e9 / hbm, 4),
+                       "algorithmic_bytes": int(run.alg_bytes), "fma_per_layer": int(run.fmas),
+                       "steps": K, "repeats": t["repeats"], "launch": t["launch"], "clocks": t["clocks"],
+                       "status": int(run.buf["status"].item())}
+                ent.update(bound_of(run, us, hbm, mhz, sms))
+                sweep.append(ent)
+                del run
+                torch.cuda.empty_cache()
+            except (RuntimeError, torch.cuda.OutOfMemoryError) as ex:
+                sweep.append({"workload": wl, "rows": Rs, "act": act, "error": str(ex)[:200]})
 
     # ---------------------------------------------------------------- CPU oracle baseline
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_full_layer(cfg, inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds,
+        cpu = cpu_baseline_full_layer(cfg, main.inp, packed_seed=cfg["seed"], dev=dev, seconds=args.cpu_seconds,
                                       sample_rows=8 if R > 64 else None)
 
-    hbm, hbm_src = peaks()
-    kern_avg_ms = statistics.fmean(kern_ms)
-    if fused and graph is not None:
-        # one launch per step: the step time bounds the launch's duration from above, and the
-        # event brackets of the replay add their own delay
-        kern_avg_ms = min(kern_avg_ms, elapsed_ms / K)
-    P = R * k
-    act_b = 1 if kind == synth.ACT_E4M3 else 2
-    x_b = R * H * act_b + (R * (H // 32) if kind == synth.ACT_E4M3 else 0)
-    h_b = P * I * act_b + (P * (I // 32) if kind == synth.ACT_E4M3 else 0)
-    tensor = None
-    if fused:
-        # weights of the distinct experts once, activations in, h written and read back, the
-        # expert outputs written and read back by the combine, ids/weights, and y
+    us_per_layer = 1000.0 * elapsed_ms / K
+    kb = bound_of(main, us_per_layer, hbm, sm_mhz, sms)
+    if main.fused:
         kern_name = "moe_rows (route+gate/up+down+combine, one launch)"
-        kern_alg = wbytes + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
-    elif chunk:
-        # gate/up weights of the distinct experts once, the activation rows in, h out; the
-        # tensor work is 2 * P * 2I * H flops (E4M3 x E2M1, fp8-class rate)
+        kern_alg = main.alg_bytes
+    elif main.chunk:
         kern_name = "upc_chunk (activation rows into pair order + gate/up chunk kernel, tcgen05 mxf8f6f4)"
-        kern_alg = n_distinct * 2 * I * (H // 2 + H // 32) + x_b + h_b
-        flops = 2.0 * P * 2 * I * H
-        tpeak, tsrc = tensor_peak_fp8()
-        tensor = {"achieved_tflops": round(flops / (kern_avg_ms * 1e-3) / 1e12, 1), "peak_tflops": tpeak,
-                  "peak_source": tsrc, "frac": round(flops / (kern_avg_ms * 1e-3) / 1e12 / tpeak, 4),
-                  "flops_per_launch": flops}
+        kern_alg = main.n_distinct * 2 * I * (H // 2 + H // 32)
     else:
         kern_name = "upc_rows"
-        kern_alg = n_distinct * 2 * I * (H // 2 + H // 32) + x_b + h_b
-    achieved = kern_alg / (kern_avg_ms * 1e-3) / 1e9
-    bound = "hbm"
-    if tensor is not None and tensor["flops_per_launch"] / (tensor["peak_tflops"] * 1e12) > kern_alg / (hbm * 1e9):
-        bound = "tensor"
-    us_per_layer = 1000.0 * elapsed_ms / (K * world)
+        kern_alg = main.n_distinct * 2 * I * (H // 2 + H // 32)
+    achieved = kern_alg / (kern_ms * 1e-3) / 1e9
+    tensor = None
+    if main.chunk:
+        flops = 2.0 * R * k * 2 * I * H
+        tpeak, tsrc = tensor_peak_fp8()
+        tensor = {"achieved_tflops": round(flops / (kern_ms * 1e-3) / 1e12, 1), "peak_tflops": tpeak,
+                  "peak_source": tsrc, "frac": round(flops / (kern_ms * 1e-3) / 1e12 / tpeak, 4),
+                  "flops_per_launch": flops}
+    rbound = "hbm" if not main.fused else ("alu" if kb["bound"] == "alu" else "hbm")
+    roof = {"kernel": kern_name, "bound": rbound, "achieved": round(achieved, 1), "peak": hbm, "peak_source": hbm_src,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4), "algorithmic_bytes_per_launch": int(kern_alg),
+            "avg_launch_us": round(1000 * kern_ms, 3), "launch_timing": kern_how,
+            "traffic": (profiled_traffic("upc_chunk_%s_%drow" % (args.workload, R), ("tfx_chunk.cu", "tfx_common.cuh"))
+                        if main.chunk else profiled_traffic("%s_rows_%s_%drow" % ("fused" if main.fused else "upc",
+                                                                                  args.workload, R))),
+            "tensor": tensor}
+    if rbound == "alu":
+        # the fp32 chains' multiply-adds bind: the fraction is of the fma rate, stated beside
+        roof.update({"achieved": round(main.fmas / (kern_ms * 1e-3) / 1e12, 3), "unit": "T fma/s",
+                     "peak": round(fma_peak(sms, sm_mhz) / 1e12, 3), "peak_source": kb["alu_peak"],
+                     "frac": round(main.fmas / (kern_ms * 1e-3) / fma_peak(sms, sm_mhz), 4)})
     line = {
         "metric": METRIC, "value": round(us_per_layer, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "%s: H %d, I %d, E %d, top-%d, R %d, %s activations, MXFP4 weights" % (
             args.workload, H, I, E, k, R, "E4M3" if kind == synth.ACT_E4M3 else "bf16"),
-            "rows": R, "distinct_experts": n_distinct, "weight_bytes_per_layer": wbytes,
+            "rows": R, "distinct_experts": main.n_distinct, "weight_bytes_per_layer": main.wbytes,
             "layers_rotated": L, "l2": "inputs larger than L2: %d packed layer copies rotate (%.0f MB of distinct "
-                                        "weights per rotation vs 129 MB L2)" % (L, L * wbytes / 1e6),
-            "path": "fused one-launch layer" if fused else (
-                "route + gate/up chunk + down chunk (tensor cores) + combine" if chunk
+                                        "weights per rotation vs 129 MB L2)" % (L, L * main.wbytes / 1e6),
+            "path": "fused one-launch layer" if main.fused else (
+                "route + gate/up chunk + down chunk (tensor cores) + combine" if main.chunk
                 else "route + gate/up + down + combine"),
-            "parallelism": "replicas" if world > 1 else "single GPU"},
-        "weight_gbs": round(wbytes / (us_per_layer * 1e-6) / 1e9, 1),
-        "weight_gbs_frac_of_peak": round(wbytes / (us_per_layer * 1e-6) / 1e9 / hbm, 4),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "timing": "exactly %d steps per timed region (%s), the region repeated %d times (barrier and "
+                      "synchronisation around each) for %.2f s of device time; value = median repeat / %d"
+                      % (K, tm["launch"], tm["repeats"], tm["repeats"] * tm["ms"] / 1000.0, K)},
+        "weight_gbs": round(main.wbytes / (us_per_layer * 1e-6) / 1e9, 1),
+        "weight_gbs_frac_of_peak": round(main.wbytes / (us_per_layer * 1e-6) / 1e9 / hbm, 4),
+        "bound": kb,
         "separate_kernels_us": {n: round(v, 3) for n, v in breakdown.items()},
-        "roofline": {"kernel": kern_name, "bound": bound, "achieved": round(achieved, 1), "peak": hbm,
-                     "peak_source": hbm_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                     "algorithmic_bytes_per_launch": int(kern_alg), "avg_launch_us": round(1000 * kern_avg_ms, 3),
-                     "traffic": (profiled_traffic("upc_chunk_%s_%drow" % (args.workload, R),
-                                                  ("tfx_chunk.cu", "tfx_common.cuh")) if chunk else
-                                 profiled_traffic("%s_rows_%s_%drow" % ("fused" if fused else "upc", args.workload, R))),
-                     "tensor": tensor},
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": (1 if fused else 5 if chunk else 4) * K, "clocks": clocks,
-        "status": status, "launch": "cuda graph replay" if graph is not None else "eager",
-        "kernel_timing": ("fused: one launch per step, launch duration = the smaller of the step time and the "
-                          "event-timed launch" if fused else
-                          "roofline kernel timed by CUDA events in a replay of the same steps right after the "
-                          "timed region (event nodes kept out of the timed graph)") if graph is not None else
-                         "CUDA events around every launch of the timed region",
+        "roofline": roof,
+        "sweep": sweep,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": main.launches * K, "gpu_launches_per_step": main.launches,
+        "timed_repeats": tm["repeats"], "clocks": clocks, "status": status, "launch": tm["launch"],
     }
     if rank == 0:
         print(json.dumps(line))
@@ -622,7 +767,10 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1000 * el / args.steps, 4),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "%s: H %d, I %d, E %d, top-%d, R %d, %s activations, MXFP4 weights" % (
-                args.workload, H, I, cfg["E"], k, R, "E4M3" if kind == synth.ACT_E4M3 else "bf16"), "rows": R},
+                args.workload, H, I, cfg["E"], k, R, "E4M3" if kind == synth.ACT_E4M3 else "bf16"), "rows": R,
+                "step": "a bounded sample of the layer, not a whole layer: gate/up for %d outputs and down for %d "
+                        "outputs of one routed pair; ms_per_step is that sample's time and value scales it to "
+                        "a whole layer by multiply-adds" % (NG, ND)},
             "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": "per step: gate/up for %d outputs and down for %d outputs of one routed pair "
                                        "(fp32-chain mode, one thread), scaled by multiply-adds to a whole layer of "

@@ -92,12 +92,14 @@ typedef struct {
 
 /* Optional knobs of the rows kernels (pass NULL for the defaults). None changes a bit of
  * any output; they exist for tuning and for the tests that prove it.
- *   max_pass  largest pass (rows decoded against one read of the weights): 0 = automatic
- *             from R; else 1, 2, 4 or 8 (gate/up) and 1, 2 or 4 (down).
- *   tier_mode 0 = pass sized by the rows left as on the pages (gate/up 8 if >= 7 rows
- *             left, 6 if >= 5, 4 if >= 3, else 2 or 1; down 4 if >= 3, else 2 or 1);
+ *   max_pass  largest pass (rows decoded against one read of the weights): 0 = min(R, 8)
+ *             for gate/up and min(R, 4) for down; else 1..8 (gate/up) and 1..4 (down).
+ *   tier_mode 0 = every pass takes min(rows left, max_pass) rows (sized by the rows left,
+ *             no padding);
  *             1 = every pass at max_pass (padding rows repeat the last real row, are
- *             computed and never written).
+ *             computed and never written);
+ *             2 = the pages' tiers, capped at max_pass (gate/up 8 if >= 7 rows left, 6 if
+ *             >= 5, 4 if >= 3, else 2 or 1; down 4 if >= 3, else 2 or 1), padded likewise.
  *   timeout_ns bound of every wait; 0 = 2 s. */
 typedef struct {
   int32_t max_pass;
@@ -259,7 +261,8 @@ int tfx_xp_router_grouped(int32_t rows, int32_t n_logits, int32_t top_k, const f
  * tfx_xp_combine, a row with a left-out slot (invalid id, flagged in status) combines that
  * slot's unwritten (stale) entries of out.
  * ids int32 [R][k], topk_w fp32 [R][k]; h / h_scale / out as for the separate entries; y bf16
- * [R][H]; y_f32_dbg fp32 [R][H] or NULL.
+ * [R][H]; y_f32_dbg fp32 [R][H], gu_dbg fp32 [R*k][2][I] and h_dbg fp32 [R*k][I] (as for
+ * tfx_xp_upc_rows) are debug copies, NULL to skip.
  * scratch: tfx_xp_moe_rows_scratch_bytes(d, R) bytes of device memory, 4-byte aligned, zero
  * before its first use; every call that completes returns it to zero (each counter's last
  * user clears it; a call that stopped early on TFX_ST_TIMEOUT may leave counters set, and the
@@ -267,14 +270,17 @@ int tfx_xp_router_grouped(int32_t rows, int32_t n_logits, int32_t top_k, const f
  * must not overlap on the device. The CTAs of one launch wait on one another, so the launch
  * is cooperative (all CTAs resident at once; the runtime refuses it otherwise: TFX_ELAUNCH);
  * a wait that runs out sets TFX_ST_TIMEOUT.
- * Returns TFX_EUNSUPPORTED for R*k > 256. opts->max_pass applies to gate/up (1, 2, 4 or 8);
- * the down pass is the same capped at 4. */
+ * Work is handed out one pass at a time, pass-major (every expert's first gate/up pass, then
+ * the second passes, ..., then the down passes in the same order), so consecutive passes on one
+ * CTA mostly share their activation rows.
+ * Returns TFX_EUNSUPPORTED for R*k > 256. opts->max_pass applies to gate/up (1..8); the down
+ * pass is the same capped at 4. */
 size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows);
 int tfx_xp_moe_rows(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x,
                     const uint8_t* x_scale, const int32_t* ids, const float* topk_w, int32_t* offs,
                     int32_t* pair_row, int32_t* pair_slot, int32_t* active, int32_t* n_active, void* h,
-                    uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* scratch,
-                    int32_t* status, const tfx_rows_opts* opts, void* stream);
+                    uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, float* gu_dbg, float* h_dbg,
+                    int32_t* scratch, int32_t* status, const tfx_rows_opts* opts, void* stream);
 
 /* The one-launch layer without caller scratch (no counterpart on the pages: it is an
  * interface for callers that cannot allocate). Some callers cannot call cudaMalloc: code

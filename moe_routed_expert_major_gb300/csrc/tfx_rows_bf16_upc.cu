@@ -1,0 +1,7 @@
+// tfx_rows_bf16_upc.cu -- the rows engine's kernel instances for bf16 activations, upc rows (tfx_rows.cuh);
+// one translation unit per activation format and phase so that they compile in parallel.
+#include "tfx_rows.cuh"
+
+namespace tfx {
+template int dispatch<TFX_ACT_BF16, PH_UPC>(const RowsParams&, int, cudaStream_t);
+}  // namespace tfx

@@ -65,7 +65,7 @@ def load():
             "tfx_xp_combine": (ctypes.c_int, [Dims, _I32, _P, _P, _P, _P, _P]),
             "tfx_xp_moe_rows_scratch_bytes": (ctypes.c_size_t, [Dims, _I32]),
             "tfx_xp_moe_rows": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                               _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
+                                               _P, _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_moe_rows_noalloc": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_router": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P]),
@@ -177,12 +177,13 @@ def tfx_xp_moe_rows_scratch_bytes(d, rows):
 
 
 def tfx_xp_moe_rows(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, h, h_scale, out, y, scratch, status,
-                    y_f32=None, opts=None):
+                    y_f32=None, opts=None, gu_dbg=None, h_dbg=None):
     o = ctypes.byref(opts) if opts is not None else None
     _check(load().tfx_xp_moe_rows(d, rows, kind, _ptr(packed), _ptr(x), _ptr(x_scale), _ptr(ids), _ptr(topk_w),
                                   _ptr(rt["offs"]), _ptr(rt["pair_row"]), _ptr(rt["pair_slot"]), _ptr(rt["active"]),
                                   _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out), _ptr(y), _ptr(y_f32),
-                                  _ptr(scratch), _ptr(status), o, _stream()), "tfx_xp_moe_rows")
+                                  _ptr(gu_dbg), _ptr(h_dbg), _ptr(scratch), _ptr(status), o, _stream()),
+           "tfx_xp_moe_rows")
 
 
 def tfx_xp_moe_rows_noalloc(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, h, h_scale, out, y, status,
@@ -260,7 +261,7 @@ def alloc_layer(R, H, I, E, k, kind, device, debug=False, chunk=False):
 def layer_fused(d, R, kind, packed, x, x_scale, ids, w, buf, opts=None):
     """One MoE layer of R rows in a single launch (tfx_xp_moe_rows)."""
     tfx_xp_moe_rows(d, R, kind, packed, x, x_scale, ids, w, buf["route"], buf["h"], buf["h_scale"], buf["out"],
-                    buf["y"], buf["scratch"], buf["status"], buf["y_f32"], opts)
+                    buf["y"], buf["scratch"], buf["status"], buf["y_f32"], opts, buf["gu_dbg"], buf["h_dbg"])
 
 
 def layer_chunk(d, R, kind, packed, x, x_scale, ids, w, buf, opts=None):

@@ -22,7 +22,9 @@ def rows_and_route(lib):
     assert L.tfx_xp_upc_rows(d, 1, 0, None, st, st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
     assert L.tfx_xp_upc_rows(d, 1, 0, st, ctypes.c_void_p(17), st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
     assert L.tfx_xp_upc_rows(d, 1, 7, st, st, st, ctypes.byref(rt), st, st, None, None, st, None, None) == -1
-    o = tfx.opts_struct(max_pass=3)
+    o = tfx.opts_struct(max_pass=9)
+    assert L.tfx_xp_upc_rows(d, 1, 0, st, st, st, ctypes.byref(rt), st, st, None, None, st, ctypes.byref(o), None) == -1
+    o = tfx.opts_struct(max_pass=3, tier_mode=3)
     assert L.tfx_xp_upc_rows(d, 1, 0, st, st, st, ctypes.byref(rt), st, st, None, None, st, ctypes.byref(o), None) == -1
     o = tfx.opts_struct(max_pass=8)
     assert L.tfx_xp_down_rows(d, 1, 0, st, st, st, ctypes.byref(rt), st, st, ctypes.byref(o), None) == -1

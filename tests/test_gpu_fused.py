@@ -1,6 +1,10 @@
-"""The one-launch layer (tfx_xp_moe_rows) against the four separate launches: identical row
-lists, h, d and combine output bit for bit, on small and full-width layers, every pass-size
-setting and the routing/NaN matrix; its scratch returns to zero after every call."""
+"""The one-launch layer (tfx_xp_moe_rows), the launch the benchmark times: against the CPU
+oracle at every benchmarked configuration (full DeepSeek-class widths: g, u, d and the combine
+bit for bit against the fp32-chain oracle, h within the float64 bound and quantised by the
+oracle's rule, every final value within the float64 bound), and against the four separate
+launches (identical row lists, h, d and combine output bit for bit) on small and full-width
+layers, every pass-size setting and the routing/NaN matrix; its scratch returns to zero after
+every call."""
 import numpy as np
 import pytest
 
@@ -15,6 +19,7 @@ if not torch.cuda.is_available():
 import gpu_util as gu  # noqa: E402
 from moe_routed_expert_major_gb300 import tfx  # noqa: E402
 from test_gpu_invariance import make_case, ROWS  # noqa: E402
+from test_gpu_parity import check_layer  # noqa: E402
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -59,8 +64,8 @@ def test_fused_matrix_and_pass_sizes(kind):
                 gu.assert_same_layer(fus, sep, lay)
     lay = make_case(lay0, kind, "same", 16, False, seed=5)
     sep = gu.run_layer(lay, packed, debug=True)
-    for mp in (1, 2, 4, 8):
-        for tm in (0, 1):
+    for mp in (1, 2, 3, 4, 5, 6, 7, 8):
+        for tm in (0, 1, 2):
             fus, _ = gu.run_layer_fused(lay, packed, opts=tfx.opts_struct(max_pass=mp, tier_mode=tm))
             gu.assert_same_layer(fus, sep, lay)
 
@@ -91,4 +96,41 @@ def test_fused_full_width(name, R):
     fus, scratch = gu.run_layer_fused(lay, packed)
     assert sep["status"] == 0 and fus["status"] == 0
     gu.assert_same_layer(fus, sep, lay)
+    assert int(scratch.abs().sum().item()) == 0
+
+
+_FULL = {}
+
+
+def _full_packed(cfg):
+    """One full-width weight set per seed (canonical copy for the oracle, packed for the launch)."""
+    key = cfg["seed"]
+    if key not in _FULL:
+        dw = synth.weights_torch(cfg["E"], cfg["H"], cfg["I"], cfg["seed"], gu.DEV)
+        d = tfx.dims(cfg["H"], cfg["I"], cfg["E"], cfg["k"])
+        _FULL[key] = (dw, gu.pack(d, dw))
+    return _FULL[key]
+
+
+BENCH_CONFIGS = ([("decode", 1, synth.ACT_E4M3)] + [("shared", R, synth.ACT_E4M3) for R in (2, 3, 4, 5, 8, 16)] +
+                 [("apart", R, kind) for R in (2, 4, 8, 16) for kind in (synth.ACT_BF16, synth.ACT_E4M3)])
+
+
+@pytest.mark.parametrize("name,R,kind", BENCH_CONFIGS,
+                         ids=["%s-%d-%s" % (n, R, "bf16" if k == synth.ACT_BF16 else "e4m3") for n, R, k in BENCH_CONFIGS])
+def test_fused_matches_oracle_at_benchmarked_configs(orc, name, R, kind):
+    """The benchmarked launch itself against the oracle: every output of the one-row decode
+    layer, and rows 0, R/2 and R-1 of the multi-row layers."""
+    cfg = synth.workload(name, kind=kind)
+    dw, packed = _full_packed(cfg)
+    lay = dict(H=cfg["H"], I=cfg["I"], E=cfg["E"], k=cfg["k"], kind=kind)
+    for n, t in dw.items():
+        lay[n] = gu.LazyExperts(t)
+    lay.update(synth.make_inputs(cfg, R=R))
+    res, scratch = gu.run_layer_fused(lay, packed, canary=0x6B)
+    assert res["status"] == 0
+    rows = None if R == 1 else sorted({0, R // 2, R - 1})
+    check_layer(orc, lay, res, rows=rows)
+    used = int(res["route"]["offs"][-1])
+    assert used == R * cfg["k"]
     assert int(scratch.abs().sum().item()) == 0

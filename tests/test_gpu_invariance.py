@@ -111,8 +111,8 @@ def test_pass_size_changes_no_bit(weights, kind):
     for routing, R in (("same", 16), ("same", 5), ("random", 16), ("same", 3)):
         lay = make_case(base, kind, routing, R, False, seed=7 + R)
         ref = outputs_by_row(lay, gu.run_layer(lay, packed, debug=False))
-        for mp in (1, 2, 4, 8):
-            for tm in (0, 1):
+        for mp in (1, 2, 3, 4, 5, 6, 7, 8):
+            for tm in (0, 1, 2):
                 ou = tfx.opts_struct(max_pass=mp, tier_mode=tm)
                 od = tfx.opts_struct(max_pass=min(mp, 4), tier_mode=tm)
                 got = outputs_by_row(lay, gu.run_layer(lay, packed, debug=False, opts_upc=ou, opts_down=od))
