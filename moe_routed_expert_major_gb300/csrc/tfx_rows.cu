@@ -51,20 +51,11 @@ static Proj proj_of(const tfx_dims& d, bool down, const uint8_t* w) {
   p.K = down ? d.inter : d.hidden;
   p.S = (p.K + KC - 1) / KC;
   p.G = p.K / 32;
-  p.GB = 2 * p.S;
   p.units = down ? d.hidden / 64 : d.inter / 32;
   p.unit_bytes = (size_t)p.S * STAGE_B;
   p.expert_bytes = (size_t)p.units * p.unit_bytes;
   p.w = w;
   return p;
-}
-
-// Raw-buffer geometry for activation rows of width kmax (bulk copies need 16-byte multiples;
-// scales come by bulk copy only when a row of them is a 16-byte multiple and 16-byte aligned).
-static void set_raw(RowsParams& P, int kind, int kmax, int gmax) {
-  const int ab = kind == TFX_ACT_E4M3 ? 1 : 2;
-  P.raw_row = (kmax * ab + 127) & ~127;
-  P.raw_sc = kind == TFX_ACT_E4M3 ? ((gmax + 15) & ~15) : 0;
 }
 
 size_t packed_gu_bytes(const tfx_dims& d) {
@@ -133,9 +124,6 @@ extern "C" int tfx_xp_upc_rows(tfx_dims d, int32_t rows, int32_t act_kind, const
   P.hs = h_scale;
   P.gu_dbg = gu_dbg;
   P.h_dbg = h_dbg;
-  P.gbmax = P.pu.GB;
-  set_raw(P, act_kind, P.pu.K, P.pu.G);
-  P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * P.pu.units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_UPC>(P, max_items, st);
@@ -162,9 +150,6 @@ extern "C" int tfx_xp_down_rows(tfx_dims d, int32_t rows, int32_t act_kind, cons
   P.h = const_cast<void*>(h);
   P.hs = const_cast<uint8_t*>(h_scale);
   P.out = out;
-  P.gbmax = (act_kind == TFX_ACT_BF16 ? 2 : 1) * P.pd.GB;  // bf16 h is staged as fp32
-  set_raw(P, act_kind, P.pd.K, P.pd.G);
-  P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
   const int max_items = min(rows * d.top_k, d.n_experts) * P.pd.units;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (act_kind == TFX_ACT_E4M3) return dispatch<TFX_ACT_E4M3, PH_DOWN>(P, max_items, st);
@@ -214,11 +199,7 @@ static int moe_rows_prepare(tfx_dims d, int32_t rows, int32_t act_kind, const ui
   P.gu_dbg = gu_dbg;
   P.h_dbg = h_dbg;
   P.scratch = scratch;
-  P.gbmax = max(P.pu.GB, (act_kind == TFX_ACT_BF16 ? 2 : 1) * P.pd.GB);  // bf16 h is staged as fp32
   P.route_ints = fused_route_ints(d.n_experts, rows, d.top_k, instance_warps(P.cap_u));
-  set_raw(P, act_kind, max(P.pu.K, P.pd.K), max(P.pu.G, P.pd.G));
-  P.sc_tma_u = act_kind == TFX_ACT_E4M3 && P.pu.G % 16 == 0 && aligned16(x_scale);
-  P.sc_tma_d = act_kind == TFX_ACT_E4M3 && P.pd.G % 16 == 0 && aligned16(h_scale);
   max_items = min(rows * d.top_k, d.n_experts) * (P.pu.units + P.pd.units);
   return TFX_OK;
 }

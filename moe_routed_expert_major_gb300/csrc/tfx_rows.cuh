@@ -12,26 +12,30 @@
 // from +0 in k order, one scaled fma into accumulator (group mod 8), then the eight-way tree.
 //
 // GB300 mapping:
-//   * one producer warp streams 17,408-byte stages (64 weight rows x 512 k of codes, then their
-//     scales: contiguous in the packed layout) into a ring of shared-memory slots with
-//     cp.async.bulk + mbarrier (every wait bounded);
-//   * consumer warps: lane (t & 7) of an octet owns accumulator lane j = group mod 8 of its
-//     output columns, so the eight-way tree is three xor-shuffles. A lane handles groups j and
-//     j + 8 of each stage. Kernels whose passes hold at most 2 rows run 8 consumer warps (two
-//     columns a lane, two CTAs an SM); kernels with longer passes run 16 consumer warps (one
-//     column a lane, one CTA an SM), so that the fma-bound passes of many rows have four
-//     consumer warps per scheduler and at most 104 registers a thread;
-//   * E2M1 codes decode with cvt.rn.f16x2.e2m1x2; activations sit in shared memory as f16
-//     (exact for E4M3; bf16 rows are shifted per 32-group by a power of two so that they are
-//     exact in f16, with an exact fp32 fallback for groups that do not fit); the chain runs on
-//     fma.rn.f32.f16 (fp32 accumulate, one rounding per step).
-//   * The fused layer launch (cooperative: all CTAs resident) computes the row lists in shared
+//   * a ring of shared-memory slots, one per stage of 512 k: the producer warp bulk-copies the
+//     stage's weights (64 rows x 512 k of codes, then their scales: 17,408 contiguous bytes of
+//     the packed layout, per packed unit of the item) and the pass's activation rows for the
+//     same 512 k (cp.async.bulk + mbarrier, every wait bounded);
+//   * the stager warp converts each slot's activation chunk into f16 (E4M3: exact; bf16 rows
+//     shifted per 32-group by a power of two so that they are exact in f16, with an exact fp32
+//     fallback for groups that do not fit; bf16 h of the down passes as fp32) and completes the
+//     slot. Shared memory thus holds a few stages, whatever the pass's rows and K;
+//   * consumer warps: lane (t & 7) of an octet owns accumulator lane j = group mod 8 of two
+//     output columns (the gate and up rows of one output, or two down rows), so the eight-way
+//     tree is three xor-shuffles, and every activation value read from shared memory feeds two
+//     columns. A lane handles groups j and j + 8 of each stage. E2M1 codes decode with
+//     cvt.rn.f16x2.e2m1x2; the chain runs on fma.rn.f32.f16 (fp32 accumulate, one rounding per
+//     step). One-row kernels run 8 consumer warps on one packed unit per item, two CTAs an SM;
+//     kernels with longer passes run 16 consumer warps on two packed units per item, one CTA an
+//     SM, so that the fma-bound passes of many rows have four consumer warps per scheduler;
+//   * the epilogue warp takes each pass's results (SwiGLU and the activation quantiser, or the
+//     expert outputs and, in the fused launch, the combine) while the consumers go on;
+//   * the fused layer launch (cooperative: all CTAs resident) computes the row lists in shared
 //     memory in every CTA and hands out work units of one pass each, pass-major: first every
 //     expert's first gate/up pass, then the second passes, ..., then the down passes in the
-//     same order (each waits, bounded, for its expert's gate/up units). A CTA's consecutive
-//     units then mostly share their rows, whose staged activations it keeps. Each (row,
-//     64-output block) is combined in the CTA whose down unit completes the row's last slot.
-//     Completion counters live in caller scratch; each counter's last user returns it to zero.
+//     same order (each waits, bounded, for its expert's gate/up units). Each (row, 64-output
+//     block) is combined in the CTA whose down unit completes the row's last slot. Completion
+//     counters live in caller scratch; each counter's last user returns it to zero.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -47,7 +51,7 @@ namespace tfx {
 
 constexpr int KC = 512;                          // k per stage
 constexpr int GPS = KC / 32;                     // groups per stage
-constexpr int TROWS = 64;                        // weight rows per stage
+constexpr int TROWS = 64;                        // weight rows per packed unit and stage
 constexpr int CODE_B = KC / 2;                   // code bytes per row per stage
 constexpr int STAGE_B = TROWS * (CODE_B + GPS);  // 17,408
 constexpr int MAX_NSTAGE = 8;
@@ -55,25 +59,31 @@ constexpr int FUSED_MAX_PAIRS = 256;
 constexpr int MAX_PASS_U = 8;                    // longest gate/up pass
 constexpr int MAX_PASS_D = 4;                    // longest down pass
 constexpr int QD = 4;                            // claimed-item queue depth (fused)
+constexpr int UNITS_IN_FLIGHT = 8;               // weight stages (of one packed unit) in flight per SM
 
 enum { PH_UPC = 1, PH_DOWN = 2, PH_FUSED = 3 };
 
 // Shape of a kernel instance whose passes hold at most MAXR rows.
 template <int MAXR>
 struct Cfg {
-  static constexpr int NCW = MAXR <= 2 ? 8 : 16;     // consumer warps
-  static constexpr int COLS = 64 / (NCW * 4);        // output columns per consumer lane
-  static constexpr int NT = NCW * kWarp + 3 * kWarp;  // + producer, stager and epilogue warps
-  static constexpr int MINB = MAXR <= 2 ? 2 : 1;     // resident CTAs per SM
-  // registers a thread may take with MINB CTAs of NT threads resident: each of the SM's four
-  // schedulers holds a quarter of the 65,536 registers and up to ceil(warps / 4) warps of a
-  // CTA (whole 8-register steps)
-  static constexpr int MAXREG = (16384 / (MINB * ((NT / kWarp + 3) / 4) * kWarp)) / 8 * 8;
-  static constexpr int W_PROD = NCW, W_HELP = NCW + 1, W_EPI = NCW + 2;
+  static constexpr int NCW = MAXR <= 1 ? 8 : 16;     // consumer warps
+  static constexpr int UPI = NCW / 8;                // packed units (64 weight rows each) per item
+  static constexpr int NSTG = 2;                     // stager warps (alternate stages)
+  static constexpr int NT = NCW * kWarp + (2 + NSTG) * kWarp;  // + producer, stagers and epilogue warps
+  static constexpr int MINB = MAXR <= 1 ? 2 : 1;     // resident CTAs per SM
+  static constexpr int W_PROD = NCW, W_HELP = NCW + 1, W_EPI = NCW + 1 + NSTG;
+};
+
+// Bytes per activation row of a stage in a slot, converted (f16, or fp32 for the bf16 down
+// passes, the bf16 kind reserving the larger), and of its group multipliers.
+template <int KIND>
+struct SlotRow {
+  static constexpr int ACT = KIND == TFX_ACT_E4M3 ? 2 * KC : 4 * KC;
+  static constexpr int XM = 4 * GPS;
 };
 
 struct Proj {
-  int K, S, G, GB, units;  // reduction length, stages, groups, group blocks of 8 (= 2S), items/expert
+  int K, S, G, units;  // reduction length, stages, groups, packed units per expert
   size_t unit_bytes, expert_bytes;
   const uint8_t* w;
 };
@@ -82,12 +92,7 @@ struct RowsParams {
   int H, I, E, k, R;
   Proj pu, pd;
   int cap_u, cap_d;     // longest pass of gate/up and of down (rows)
-  int nstage;
-  int nxb;              // activation buffers in shared memory (2: the next pass stages while this one runs)
-  int use_raw;          // 1: activation rows arrive by bulk copy into a shared-memory raw buffer
-  int raw_row, raw_sc;  // raw buffer bytes per row (128-aligned) and per row of scales (16-aligned)
-  int sc_tma_u, sc_tma_d;  // scales of gate/up (x) / down (h) rows come by bulk copy too
-  int gbmax;            // group blocks allotted per activation row in shared memory
+  int nstage;           // ring slots
   int route_ints;       // shared-memory ints of the in-kernel route and pass lists (fused)
   const void* x;        // token activations [R][H]
   const uint8_t* xs;    // E8M0 scales [R][H/32] (E4M3)
@@ -102,8 +107,8 @@ struct RowsParams {
   uint16_t* y;          // fused: [R][H] bf16
   float* y32;           // fused: [R][H] or null
   int32_t* scratch;     // fused: [0] unused, [1] work counter, [2..E+1] gate/up units done per
-                        //        active expert, [E+2..2E+1] down units past their wait per active
-                        //        expert, then [R][H/64] slots written per (row, block)
+                        //        active expert, [E+2..2E+1] stager passes of down units past their
+                        //        wait per active expert, then [R][H/64] slots written per (row, block)
   int32_t* status;
   int tier_mode;        // 0: passes of min(rows left, cap); 1: every pass at cap; 2: the pages' tiers
   uint64_t timeout_ns;
@@ -116,23 +121,25 @@ __host__ __device__ inline int fused_route_ints(int E, int R, int k, int nw) {
 }
 
 // ---------------------------------------------------------------- shared-memory layout
+// bars: full[8], empty[8], efull[2], eempty[2], qfull[4], qempty[4]; ctrl: abort flag and the
+// claimed-item queue; epi: two result buffers [maxr][64 upi] fp32; route: the fused launch's
+// lists; then the ring of slots: [upi weight stages | maxr converted activation rows | maxr x 16
+// group multipliers].
 struct Layout {
-  int bars, ctrl, pdesc, epi, route, ring, xs, xm, xs_stride, xm_stride, raw, total;
+  int bars, ctrl, epi, route, ring, slot, w, act, xm, total;
 };
-__host__ __device__ inline Layout layout_of(const RowsParams& p, int maxr) {
+__host__ __device__ inline Layout layout_of(const RowsParams& p, int maxr, int upi, int act_row) {
   Layout L;
-  L.bars = 0;      // full[8], empty[8], xfull[2], xempty[2], efull[2], eempty[2], rawfull, qfull[4], qempty[4]
-  L.ctrl = 384;    // abort flag, then the claimed-item queue ids
-  L.pdesc = 448;   // two pass descriptors: prow[8], ppair[8]
-  L.epi = 640;     // two float [8][64] result buffers
-  L.route = 4736;  // fused: ints
+  L.bars = 0;
+  L.ctrl = 384;
+  L.epi = 512;
+  L.route = L.epi + 2 * maxr * 64 * upi * 4;
   L.ring = (L.route + 4 * p.route_ints + 127) & ~127;
-  L.xs = L.ring + p.nstage * STAGE_B;
-  L.xs_stride = maxr * p.gbmax * 512;
-  L.xm = L.xs + p.nxb * L.xs_stride;
-  L.xm_stride = maxr * p.gbmax * 8 * 4;
-  L.raw = (L.xm + p.nxb * L.xm_stride + 127) & ~127;
-  L.total = L.raw + (p.use_raw ? maxr * (p.raw_row + p.raw_sc) : 0);
+  L.w = 0;
+  L.act = upi * STAGE_B;
+  L.xm = L.act + maxr * act_row;
+  L.slot = (L.xm + maxr * 4 * GPS + 127) & ~127;
+  L.total = L.ring + p.nstage * L.slot;
   return L;
 }
 
@@ -149,12 +156,10 @@ __device__ __forceinline__ int tier_of(int left, int cap, int mode, bool down) {
   return t > cap ? cap : t;
 }
 
-// Byte offset in the permuted activation layout of row r, group g, 8-element chunk tc:
-// chunk ((r*GB + g/8)*4 + tc)*8 + g%8 of 16 bytes, so the eight lanes that read one chunk
-// index of eight consecutive groups touch 128 consecutive bytes.
-__device__ __forceinline__ int xoff(int r, int g, int tc, int GB) {
-  return ((((r * GB + (g >> 3)) * 4 + tc) * 8 + (g & 7)) << 4);
-}
+// Byte offset, in a converted activation row of one stage, of local group g (0..15) and
+// 8-element chunk tc: chunk ((g/8)*4 + tc)*8 + g%8 of 16 bytes, so the eight lanes that read
+// one chunk index of eight consecutive groups touch 128 consecutive bytes (fp32 rows: twice).
+__device__ __forceinline__ int xoff(int g, int tc) { return ((((g >> 3) * 4 + tc) * 8 + (g & 7)) << 4); }
 
 // Exact fp32 chain for a bf16 group whose values do not fit f16 after the shift: the
 // group's codes are decoded again, and each product of an E2M1 value with the bf16 value read
@@ -176,112 +181,138 @@ static __device__ __noinline__ float chain_bf16_exact(uint4 codes, const uint16_
   return p;
 }
 
-// Stage the activation rows of one pass into the f16 activation buffer (the NT threads of the
-// calling role). Row r is read at X8 + row(r) * xstride and its scales at XS + row(r) * sstride,
-// where row(r) = prow[r] for rows in global memory, or r for rows already bulk-copied into
-// shared memory (FROM_SMEM). Global loads go through L2 (the rows may have been written by
-// other CTAs of the same launch) and are issued in batches so that many are in flight. Groups
-// from G up to the stage boundary are zero with multiplier 1, so that lanes past the end of the
-// reduction add +0 to their accumulators.
-// X32 (bf16 only): the rows are kept as fp32 values, unshifted (multiplier 1), in chunks of
-// 8 values at twice the f16 offsets; no group needs the exact fallback then.
-template <int KIND, bool FROM_SMEM, bool SC_SMEM, bool X32 = false>
-__device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const uint8_t* __restrict__ XS,
-                           size_t sstride, int K, int G, int GB, uint8_t* xs_s, float* xm_s, const int* prow,
-                           int real, int tid, int NT) {
-  const int nch = K / 8;          // chunks of 8 elements with data
-  const int nall = GB * 8 * 4;    // chunks up to the stage boundary
-  constexpr int BATCH = 8;
-  if (KIND == TFX_ACT_E4M3) {
-    const int gall = GB * 8;
-    for (int r = 0; r < real; ++r) {
-      const uint8_t* xrow = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride;
-      for (int c0 = tid; c0 < nall; c0 += BATCH * NT) {
-        uint2 v[BATCH];
+// Convert one stage (512 k from k0 = 512 s) of t activation rows, read from global memory, into
+// a slot's converted rows and group multipliers (the calling warp). Row r is X8 row rw[r]
+// (K elements) with scales XS row rw[r] (G = K/32); every load of the stage is issued before
+// its conversions, so that a stage costs one memory latency. The stage covers local groups g < gv =
+// min(16, G - 16 s) with data; later groups are zero with multiplier 1, so that lanes past the
+// end of the reduction add +0 to their accumulators. COH: the rows were written in this launch
+// (h of the fused down passes) and are read at L2; else (x) they may stay in L1.
+//   MODE 0 (E4M3): codes -> f16 (exact); multipliers from the E8M0 scales.
+//   MODE 1 (bf16): one lane per 32-group shifts it by 2^sigma, mapping its largest magnitude
+//     into [2^15, 2^16): the group is exact in f16 and its chain equals the unshifted fp32
+//     chain times 2^sigma when every finite nonzero value has exponent in [e_max - 32, e_max],
+//     e_max <= 119 and e_min >= -141 (products and partial sums then stay in fp32's normal
+//     range, or on its subnormal grid, on both sides); the multiplier is 2^-sigma then, else 0,
+//     which sends the group to the exact fallback.
+//   MODE 2 (bf16 as fp32): values unshifted in 32-byte chunks, multiplier 1.
+template <bool COH, typename V>
+__device__ __forceinline__ V ld_act(const void* p) {
+  return COH ? __ldcg(reinterpret_cast<const V*>(p)) : __ldg(reinterpret_cast<const V*>(p));
+}
+// Row rr of MR row indices held in registers (rr uniform per call site, so no local memory).
+template <int MR>
+__device__ __forceinline__ int pick_row(const int (&rw)[MR], int rr) {
+  int v = rw[0];
 #pragma unroll
-        for (int q = 0; q < BATCH; ++q) {
-          const int c = c0 + q * NT;
-          v[q] = make_uint2(0u, 0u);
-          if (c < nch)
-            v[q] = FROM_SMEM ? *reinterpret_cast<const uint2*>(xrow + 8 * c)
-                             : __ldcg(reinterpret_cast<const uint2*>(xrow + 8 * c));
-        }
+  for (int r = 1; r < MR; ++r) v = rr == r ? rw[r] : v;
+  return v;
+}
+// A stage's activation data in registers, between its loads and its conversion.
+template <int KIND, int MODE, int MR>
+struct StageRegs {
+  static constexpr int NQ = (MR + 1) / 2;           // items of (row, group) a lane holds (MODE 1)
+  uint2 v0[MODE == 0 ? MR : 1][2];                  // MODE 0: codes
+  uint32_t sv[MODE == 0 ? NQ : 1];                  // MODE 0: scale codes
+  // MODE 1 (bf16 rows shifted into f16) keeps nothing here: its loads run in the store phase,
+  // two (row, group) items at a time, to bound the registers
+  uint4 v2[MODE == 2 ? MR : 1][2];                  // MODE 2: bf16 chunks
+};
+
+template <int KIND, int MODE, bool COH, int MR>
+__device__ __forceinline__ void stage_load(StageRegs<KIND, MODE, MR>& R_, const uint8_t* X8, const uint8_t* XS,
+                                           int t, int s, int K, int G, const int (&rw)[MR], int lane) {
+  constexpr int AB = KIND == TFX_ACT_E4M3 ? 1 : 2;
+  const int gv = min(GPS, G - GPS * s);
+  const size_t koff = (size_t)KC * s * AB;
+  if (MODE == 0) {
 #pragma unroll
-        for (int q = 0; q < BATCH; ++q) {
-          const int c = c0 + q * NT;
-          if (c >= nall) break;
-          uint4 o;
-          o.x = e4m3x2_to_f16x2(v[q].x);
-          o.y = e4m3x2_to_f16x2(v[q].x >> 16);
-          o.z = e4m3x2_to_f16x2(v[q].y);
-          o.w = e4m3x2_to_f16x2(v[q].y >> 16);
-          *reinterpret_cast<uint4*>(xs_s + xoff(r, c >> 2, c & 3, GB)) = o;
-        }
-      }
-      const uint8_t* srow = XS + (size_t)(SC_SMEM ? r : prow[r]) * sstride;
-      for (int g0 = tid; g0 < gall; g0 += BATCH * NT) {
-        uint32_t sv[BATCH];
+    for (int r = 0; r < MR; ++r) {
+      const uint8_t* rr = X8 + (size_t)rw[r] * K + koff;
 #pragma unroll
-        for (int q = 0; q < BATCH; ++q) {
-          const int g = g0 + q * NT;
-          sv[q] = 127u;
-          if (g < G) sv[q] = SC_SMEM ? srow[g] : __ldcg(srow + g);
-        }
-#pragma unroll
-        for (int q = 0; q < BATCH; ++q) {
-          const int g = g0 + q * NT;
-          if (g >= gall) break;
-          xm_s[r * gall + g] = g < G ? e8m0_to_f32(sv[q]) : 1.0f;
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        R_.v0[r][h] = make_uint2(0u, 0u);
+        if (r < t && (c >> 2) < gv) R_.v0[r][h] = ld_act<COH, uint2>(rr + 8 * c);
       }
     }
+#pragma unroll
+    for (int q = 0; q < StageRegs<KIND, MODE, MR>::NQ; ++q) {
+      const int r = 2 * q + (lane >> 4), g = lane & 15;
+      R_.sv[q] = 127u;
+      if (r < t && g < gv) R_.sv[q] = ld_act<COH, uint8_t>(XS + (size_t)pick_row(rw, r) * G + GPS * s + g);
+    }
+  } else if (MODE == 1) {
+    // loaded in stage_store
   } else {
-    // bf16: one thread converts one 32-group with a power-of-two shift 2^sigma that maps the
-    // group's largest magnitude into [2^15, 2^16). The group is exact in f16 and its chain
-    // equals the unshifted fp32 chain times 2^sigma when every finite nonzero value has
-    // exponent in [e_max - 32, e_max], e_max <= 119 and e_min >= -141 (products and partial
-    // sums then stay in fp32's normal range, or on its subnormal grid, on both sides).
-    // Otherwise the multiplier is 0 and the exact fallback runs for that group.
-    const int gall = GB * 8;
-    const int total = real * gall;
-    for (int i = tid; i < total; i += NT) {
-      const int r = i / gall, g = i - r * gall;
-      uint4 v[4];  // the group's 32 bf16 values, element 2j in the low half of word j
 #pragma unroll
-      for (int q = 0; q < 4; ++q) v[q] = make_uint4(0u, 0u, 0u, 0u);
-      if (g < G) {
-        const uint8_t* src = X8 + (size_t)(FROM_SMEM ? r : prow[r]) * xstride + 64 * g;
+    for (int r = 0; r < MR; ++r) {
+      const uint8_t* rr = X8 + (size_t)rw[r] * K * AB + koff;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          v[q] = FROM_SMEM ? *reinterpret_cast<const uint4*>(src + 16 * q)
-                           : __ldcg(reinterpret_cast<const uint4*>(src + 16 * q));
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        R_.v2[r][h] = make_uint4(0u, 0u, 0u, 0u);
+        if (r < t && (c >> 2) < gv) R_.v2[r][h] = ld_act<COH, uint4>(rr + 16 * c);
       }
-      const uint32_t* wv = reinterpret_cast<const uint32_t*>(v);
-      if (X32) {
+    }
+  }
+}
+
+template <int KIND, int MODE, bool COH, int MR>
+__device__ __forceinline__ void stage_store(const StageRegs<KIND, MODE, MR>& R_, uint8_t* act, int act_stride,
+                                            float* xm, int xm_stride, int t, int s, int K, int G, const uint8_t* X8,
+                                            const int (&rw)[MR], int lane) {
+  constexpr int AB = KIND == TFX_ACT_E4M3 ? 1 : 2;
+  const int gv = min(GPS, G - GPS * s);
+  const size_t koff = (size_t)KC * s * AB;
+  if (MODE == 0) {
 #pragma unroll
-        for (int tc = 0; tc < 4; ++tc) {
-          uint4 o0, o1;
-          o0.x = wv[4 * tc] << 16;
-          o0.y = wv[4 * tc] & 0xFFFF0000u;
-          o0.z = wv[4 * tc + 1] << 16;
-          o0.w = wv[4 * tc + 1] & 0xFFFF0000u;
-          o1.x = wv[4 * tc + 2] << 16;
-          o1.y = wv[4 * tc + 2] & 0xFFFF0000u;
-          o1.z = wv[4 * tc + 3] << 16;
-          o1.w = wv[4 * tc + 3] & 0xFFFF0000u;
-          uint4* dst = reinterpret_cast<uint4*>(xs_s + 2 * xoff(r, g, tc, GB));
-          dst[0] = o0;
-          dst[1] = o1;
-        }
-        xm_s[r * gall + g] = 1.0f;
-        continue;
+    for (int r = 0; r < MR; ++r) {
+      if (r >= t) break;
+      uint8_t* ar = act + r * act_stride;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h, g = c >> 2, tc = c & 3;
+        uint4 o;
+        o.x = e4m3x2_to_f16x2(R_.v0[r][h].x);
+        o.y = e4m3x2_to_f16x2(R_.v0[r][h].x >> 16);
+        o.z = e4m3x2_to_f16x2(R_.v0[r][h].y);
+        o.w = e4m3x2_to_f16x2(R_.v0[r][h].y >> 16);
+        *reinterpret_cast<uint4*>(ar + xoff(g, tc)) = o;
       }
-      // the exponents of the largest and of the smallest nonzero finite magnitude (magnitude bits
-      // order like the values); NaN, Inf and zeros take no part
+    }
+#pragma unroll
+    for (int q = 0; q < StageRegs<KIND, MODE, MR>::NQ; ++q) {
+      const int r = 2 * q + (lane >> 4), g = lane & 15;
+      if (r < t) xm[r * xm_stride + g] = g < gv ? e8m0_to_f32(R_.sv[q]) : 1.0f;
+    }
+  } else if (MODE == 1) {
+    constexpr int NQ = StageRegs<KIND, MODE, MR>::NQ;
+#pragma unroll
+    for (int q0 = 0; q0 < NQ; q0 += 2) {
+     uint4 v[2][4];
+#pragma unroll
+     for (int u = 0; u < 2; ++u) {
+      const int r = 2 * (q0 + u) + (lane >> 4), g = lane & 15;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[u][k] = make_uint4(0u, 0u, 0u, 0u);
+      if (q0 + u < NQ && r < t && g < gv) {
+        const uint8_t* src = X8 + (size_t)pick_row(rw, r) * K * AB + koff + 64 * g;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = ld_act<COH, uint4>(src + 16 * k);
+      }
+     }
+#pragma unroll
+     for (int u = 0; u < 2; ++u) {
+      const int r = 2 * (q0 + u) + (lane >> 4), g = lane & 15;
+      if (q0 + u >= NQ || r >= t) continue;
+      const uint32_t* wv = reinterpret_cast<const uint32_t*>(v[u]);
+      // the exponents of the largest and of the smallest nonzero finite magnitude (magnitude
+      // bits order like the values); NaN, Inf and zeros take no part
       uint32_t mxb = 0u, mnb = 0xFFFFu;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const uint32_t mag = (wv[j >> 1] >> (16 * (j & 1))) & 0x7FFFu;
+      for (int jj = 0; jj < 32; ++jj) {
+        const uint32_t mag = (wv[jj >> 1] >> (16 * (jj & 1))) & 0x7FFFu;
         const bool fin = mag - 1u < 0x7F7Fu;  // nonzero, exponent field below 255
         mxb = max(mxb, fin ? mag : 0u);
         mnb = min(mnb, fin ? mag : 0xFFFFu);
@@ -301,29 +332,55 @@ __device__ void stage_rows(const uint8_t* __restrict__ X8, size_t xstride, const
       const int s1 = min(max(sigma, -126), 127), s2 = sigma - s1;  // 2^sigma as two exact factors
       const float f1 = __uint_as_float((uint32_t)(127 + s1) << 23);
       const float f2 = __uint_as_float((uint32_t)(127 + s2) << 23);
+      uint8_t* ar = act + r * act_stride;
 #pragma unroll
       for (int tc = 0; tc < 4; ++tc) {
         uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t two = wv[4 * tc + q];
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t two = wv[4 * tc + k];
           float lo = __uint_as_float(two << 16), hi = __uint_as_float(two & 0xFFFF0000u);
           if (safe) {
             lo = __fmul_rn(__fmul_rn(lo, f1), f2);
             hi = __fmul_rn(__fmul_rn(hi, f1), f2);
           }
           const __half2 h2 = __floats2half2_rn(lo, hi);
-          o[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          o[k] = *reinterpret_cast<const uint32_t*>(&h2);
         }
-        *reinterpret_cast<uint4*>(xs_s + xoff(r, g, tc, GB)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(ar + xoff(g, tc)) = make_uint4(o[0], o[1], o[2], o[3]);
       }
       float m = 0.0f;  // 0 marks the exact fallback
-      if (g >= G) m = 1.0f;
+      if (g >= gv) m = 1.0f;
       else if (safe) {
         const int ns = -sigma;  // 2^-sigma, possibly subnormal (exact)
         m = ns >= -126 ? __uint_as_float((uint32_t)(127 + ns) << 23) : __uint_as_float(0x00400000u >> (-127 - ns));
       }
-      xm_s[r * gall + g] = m;
+      xm[r * xm_stride + g] = m;
+     }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < MR; ++r) {
+      if (r >= t) break;
+      uint8_t* ar = act + r * act_stride;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h, g = c >> 2, tc = c & 3;
+        const uint4 v = R_.v2[r][h];
+        uint4 o0, o1;
+        o0.x = v.x << 16;
+        o0.y = v.x & 0xFFFF0000u;
+        o0.z = v.y << 16;
+        o0.w = v.y & 0xFFFF0000u;
+        o1.x = v.z << 16;
+        o1.y = v.z & 0xFFFF0000u;
+        o1.z = v.w << 16;
+        o1.w = v.w & 0xFFFF0000u;
+        uint4* dst = reinterpret_cast<uint4*>(ar + 2 * xoff(g, tc));
+        dst[0] = o0;
+        dst[1] = o1;
+      }
+      if (lane < GPS) xm[r * xm_stride + lane] = 1.0f;
     }
   }
 }
@@ -511,30 +568,12 @@ __device__ void route_smem(const RowsParams& p, int* base, SRoute& rt, int tid) 
   __syncthreads();
 }
 
-// Loads from shared memory by 32-bit shared-window address (keeps per-row addresses in one
-// register each).
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float4 lds128f(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
-  return v;
-}
-__device__ __forceinline__ float lds32f(uint32_t a) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
-  return v;
-}
-
 // ---------------------------------------------------------------- one pass of T rows
 // Barriers of the shared-memory handoffs between the roles.
 struct Bars {
-  uint64_t *full, *empty;   // weight ring: producer -> consumers, consumers -> producer
-  uint64_t *xfull, *xempty; // activation buffers: helper -> consumers, consumers -> helper
-  uint64_t *efull, *eempty; // result buffers: consumers -> helper, helper -> consumers
+  uint64_t *full, *empty;   // ring slots: producer (weights landed) and stager (activations
+                            // converted) -> consumers; consumers -> producer and stager
+  uint64_t *efull, *eempty; // result buffers: consumers -> epilogue, epilogue -> consumers
 };
 
 // Bounded wait whose outcome is uniform across the calling warp; on failure the block is
@@ -566,166 +605,228 @@ struct E8m0Table {
 static __device__ const E8m0Table e8m0_table = E8m0Table();
 __device__ __forceinline__ float e8m0_lookup(uint32_t code) { return __uint_as_float(__ldg(e8m0_table.v + code)); }
 
-// Consumers: consume the pass's S weight stages against activation buffer xs_s/xm_s, release
-// the buffer, then hand the eight-way-tree results of every real row to the epilogue warp in
-// epi[r][0..63] (column c of the stage's 64 weight rows at c). A lane owns COLS columns: o and,
-// with two columns, 32 + o, where o = 4 * warp + lane / 8.
-template <int KIND, int T, int COLS, bool X32 = false>
-__device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, uint8_t* ring, const Bars& B,
-                                         int bx, int be, uint32_t eph, bool ewait, volatile int* abort_flag,
-                                         const uint8_t* xs_s, const float* xm_s, const int* prow,
-                                         const uint16_t* xraw, int real, uint32_t& it, bool& dead, float* epi) {
+// Consumers: consume the pass's S stages, then hand the eight-way-tree results of every real
+// row to the epilogue warp in epi[r][0..64 upi): lane (o = 4 warp + lane / 8, j = lane % 8)
+// owns rows rr = o % 32 and 32 + rr of packed unit o / 32 of the item (the gate and up rows of
+// one output, or two down rows), results at 64 (o / 32) + rr and + 32. SEQ: the two groups of
+// a stage run one after the other (fewer live registers for long passes); else interleaved.
+template <int KIND, int T, int UPI, bool X32, bool SEQ>
+__device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, const uint8_t* smem, const Layout& Ly,
+                                         const Bars& B, int be, uint32_t eph, bool ewait, volatile int* abort_flag,
+                                         const int* r_prow, int pos, int real, bool dn, uint32_t& it, bool& dead,
+                                         float* epi) {
+  using SR = SlotRow<KIND>;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int j = lane & 7, o = (warp << 2) | (lane >> 3);
-  int col[COLS];
+  const int uu = o >> 5, rr = o & 31;
+  constexpr int XB = X32 ? 2 : 1;  // converted bytes per f16 position
+  float acc0[T], acc1[T];
 #pragma unroll
-  for (int c = 0; c < COLS; ++c) col[c] = o + 32 * c;
-  const int NST = P.nstage, GB = pj.GB;
-  float acc[COLS][T];
-  // shared-window addresses of each row's activations (lane's chunk j) and group multipliers:
-  // the buffer holds all T rows of the pass (padding rows staged as copies of the last real
-  // row), so row r sits at a fixed offset from row 0
-  const uint32_t xs_a = smem_addr(xs_s) + (X32 ? 2 : 1) * j * 16, xm_a = smem_addr(xm_s) + 4 * j;
-  const uint32_t xrs = (X32 ? 2 : 1) * GB * 512, xms = 4 * GB * 8;  // bytes per row
+  for (int r = 0; r < T; ++r) {
+    acc0[r] = 0.0f;
+    acc1[r] = 0.0f;
+  }
+  constexpr int xrs = SlotRow<KIND>::ACT;  // bytes per activation row of a slot
+  constexpr int xms = GPS;                  // multipliers per row
+  const uint8_t* ring = smem + Ly.ring;
+  // group multiplier m of row r and local group g, and the fallback's exact chain for bf16
+  auto fold = [&](int r, int g, float p0, float p1, float s0, float s1, uint4 c0, uint4 c1, const float* xm,
+                  int gglob) {
+    const float m = xm[r * xms + g];
+    if (KIND == TFX_ACT_E4M3) {
+      acc0[r] = __fmaf_rn(p0, __fmul_rn(s0, m), acc0[r]);
+      acc1[r] = __fmaf_rn(p1, __fmul_rn(s1, m), acc1[r]);
+    } else {
+      float q0, q1;
+      if (!X32 && m == 0.0f) {
+        const int src = pos + min(r, real - 1);
+        const uint16_t* xrow = reinterpret_cast<const uint16_t*>(dn ? P.h : P.x) + (size_t)(dn ? src : r_prow[src]) * pj.K;
+        q0 = chain_bf16_exact(c0, xrow, gglob);
+        q1 = chain_bf16_exact(c1, xrow, gglob);
+      } else {
+        q0 = __fmul_rn(p0, m);
+        q1 = __fmul_rn(p1, m);
+      }
+      acc0[r] = __fmaf_rn(q0, s0, acc0[r]);
+      acc1[r] = __fmaf_rn(q1, s1, acc1[r]);
+    }
+  };
+  // one group's chains of both columns for every row: p += w * x over the group's 32 k in order
+  auto chains = [&](const uint32_t* w0, const uint32_t* w1, const uint8_t* xg, float (&p0)[T], float (&p1)[T]) {
 #pragma unroll
-  for (int r = 0; r < T; ++r)
+    for (int tc = 0; tc < 4; ++tc) {
+      uint32_t a0[4], a1[4];
+      e2m1x8_to_f16x2(w0[tc], a0[0], a0[1], a0[2], a0[3]);
+      e2m1x8_to_f16x2(w1[tc], a1[0], a1[1], a1[2], a1[3]);
 #pragma unroll
-    for (int c = 0; c < COLS; ++c) acc[c][r] = 0.0f;
+      for (int r = 0; r < T; ++r) {
+        const uint8_t* xp = xg + r * xrs + XB * tc * 128;
+        if (X32) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const float4 xa = *reinterpret_cast<const float4*>(xp + 16 * hf);
+#pragma unroll
+            for (int ii = 0; ii < 2; ++ii) {
+              const int i = 2 * hf + ii;
+              const float lo = ii ? xa.z : xa.x, hi = ii ? xa.w : xa.y;
+              const __half2 h0 = *reinterpret_cast<const __half2*>(&a0[i]);
+              const __half2 h1 = *reinterpret_cast<const __half2*>(&a1[i]);
+              p0[r] = __fmaf_rn(__low2float(h0), lo, p0[r]);
+              p0[r] = __fmaf_rn(__high2float(h0), hi, p0[r]);
+              p1[r] = __fmaf_rn(__low2float(h1), lo, p1[r]);
+              p1[r] = __fmaf_rn(__high2float(h1), hi, p1[r]);
+            }
+          }
+        } else {
+          const uint4 xa = *reinterpret_cast<const uint4*>(xp);
+          const uint32_t* va = reinterpret_cast<const uint32_t*>(&xa);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            p0[r] = fma2_f16(a0[i], va[i], p0[r]);
+            p1[r] = fma2_f16(a1[i], va[i], p1[r]);
+          }
+        }
+      }
+    }
+  };
   // ring position, advanced incrementally (no division per stage)
+  const int NST = P.nstage;
   int slot = (int)(it % (uint32_t)NST);
   uint32_t ph = (it / (uint32_t)NST) & 1u;
   for (int s = 0; s < pj.S; ++s, ++it, slot = slot + 1 == NST ? 0 : slot + 1, ph ^= slot == 0 ? 1u : 0u) {
     if (warp_wait(&B.full[slot], ph, P, abort_flag, dead)) {
-      const uint8_t* tile = ring + (size_t)slot * STAGE_B;
+      const uint8_t* sb = ring + (size_t)slot * Ly.slot;
+      const uint8_t* tile = sb + uu * STAGE_B;
       const uint8_t* sc = tile + TROWS * CODE_B;
-      uint4 cA[COLS], cB[COLS];
-      float sA[COLS], sB[COLS];
+      const uint8_t* xa_base = sb + Ly.act + XB * j * 16;
+      const float* xm = reinterpret_cast<const float*>(sb + Ly.xm);
+      const uint4 cA0 = *reinterpret_cast<const uint4*>(tile + rr * CODE_B + 16 * j);
+      const uint4 cA1 = *reinterpret_cast<const uint4*>(tile + (32 + rr) * CODE_B + 16 * j);
+      const float sA0 = e8m0_lookup(sc[rr * GPS + j]), sA1 = e8m0_lookup(sc[(32 + rr) * GPS + j]);
+      if (SEQ) {
+        float p0[T], p1[T];
 #pragma unroll
-      for (int c = 0; c < COLS; ++c) {
-        cA[c] = *reinterpret_cast<const uint4*>(tile + col[c] * CODE_B + 16 * j);
-        cB[c] = *reinterpret_cast<const uint4*>(tile + col[c] * CODE_B + 128 + 16 * j);
-        sA[c] = e8m0_lookup(sc[col[c] * GPS + j]);
-        sB[c] = e8m0_lookup(sc[col[c] * GPS + 8 + j]);
-      }
-      const int gA = s * GPS + j, gB = gA + 8;
-      float pA[COLS][T], pB[COLS][T];
+        for (int r = 0; r < T; ++r) { p0[r] = 0.0f; p1[r] = 0.0f; }
+        chains(reinterpret_cast<const uint32_t*>(&cA0), reinterpret_cast<const uint32_t*>(&cA1), xa_base, p0, p1);
 #pragma unroll
-      for (int r = 0; r < T; ++r)
+        for (int r = 0; r < T; ++r) fold(r, j, p0[r], p1[r], sA0, sA1, cA0, cA1, xm, s * GPS + j);
+        const uint4 cB0 = *reinterpret_cast<const uint4*>(tile + rr * CODE_B + 128 + 16 * j);
+        const uint4 cB1 = *reinterpret_cast<const uint4*>(tile + (32 + rr) * CODE_B + 128 + 16 * j);
+        const float sB0 = e8m0_lookup(sc[rr * GPS + 8 + j]), sB1 = e8m0_lookup(sc[(32 + rr) * GPS + 8 + j]);
 #pragma unroll
-        for (int c = 0; c < COLS; ++c) { pA[c][r] = 0.0f; pB[c][r] = 0.0f; }
+        for (int r = 0; r < T; ++r) { p0[r] = 0.0f; p1[r] = 0.0f; }
+        chains(reinterpret_cast<const uint32_t*>(&cB0), reinterpret_cast<const uint32_t*>(&cB1), xa_base + XB * 512,
+               p0, p1);
 #pragma unroll
-      for (int tc = 0; tc < 4; ++tc) {
-        uint32_t a[COLS][4], b[COLS][4];
+        for (int r = 0; r < T; ++r) fold(r, j + 8, p0[r], p1[r], sB0, sB1, cB0, cB1, xm, s * GPS + 8 + j);
+      } else {
+        const uint4 cB0 = *reinterpret_cast<const uint4*>(tile + rr * CODE_B + 128 + 16 * j);
+        const uint4 cB1 = *reinterpret_cast<const uint4*>(tile + (32 + rr) * CODE_B + 128 + 16 * j);
+        const float sB0 = e8m0_lookup(sc[rr * GPS + 8 + j]), sB1 = e8m0_lookup(sc[(32 + rr) * GPS + 8 + j]);
+        float pA0[T], pA1[T], pB0[T], pB1[T];
 #pragma unroll
-        for (int c = 0; c < COLS; ++c) {
-          e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(&cA[c])[tc], a[c][0], a[c][1], a[c][2], a[c][3]);
-          e2m1x8_to_f16x2(reinterpret_cast<const uint32_t*>(&cB[c])[tc], b[c][0], b[c][1], b[c][2], b[c][3]);
+        for (int r = 0; r < T; ++r) { pA0[r] = 0.0f; pA1[r] = 0.0f; pB0[r] = 0.0f; pB1[r] = 0.0f; }
+        const uint32_t* wA0 = reinterpret_cast<const uint32_t*>(&cA0);
+        const uint32_t* wA1 = reinterpret_cast<const uint32_t*>(&cA1);
+        const uint32_t* wB0 = reinterpret_cast<const uint32_t*>(&cB0);
+        const uint32_t* wB1 = reinterpret_cast<const uint32_t*>(&cB1);
+#pragma unroll
+        for (int tc = 0; tc < 4; ++tc) {
+          uint32_t a0[4], a1[4], b0[4], b1[4];
+          e2m1x8_to_f16x2(wA0[tc], a0[0], a0[1], a0[2], a0[3]);
+          e2m1x8_to_f16x2(wA1[tc], a1[0], a1[1], a1[2], a1[3]);
+          e2m1x8_to_f16x2(wB0[tc], b0[0], b0[1], b0[2], b0[3]);
+          e2m1x8_to_f16x2(wB1[tc], b1[0], b1[1], b1[2], b1[3]);
+#pragma unroll
+          for (int r = 0; r < T; ++r) {
+            const uint8_t* xp = xa_base + r * xrs + XB * tc * 128;
+            if (X32) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {  // four values of each group at a time
+                const float4 xa = *reinterpret_cast<const float4*>(xp + 16 * hf);
+                const float4 xb = *reinterpret_cast<const float4*>(xp + 1024 + 16 * hf);
+#pragma unroll
+                for (int ii = 0; ii < 2; ++ii) {
+                  const int i = 2 * hf + ii;
+                  const float xa_lo = ii ? xa.z : xa.x, xa_hi = ii ? xa.w : xa.y;
+                  const float xb_lo = ii ? xb.z : xb.x, xb_hi = ii ? xb.w : xb.y;
+                  const __half2 wa0 = *reinterpret_cast<const __half2*>(&a0[i]);
+                  const __half2 wa1 = *reinterpret_cast<const __half2*>(&a1[i]);
+                  const __half2 wb0 = *reinterpret_cast<const __half2*>(&b0[i]);
+                  const __half2 wb1 = *reinterpret_cast<const __half2*>(&b1[i]);
+                  pA0[r] = __fmaf_rn(__low2float(wa0), xa_lo, pA0[r]);
+                  pA0[r] = __fmaf_rn(__high2float(wa0), xa_hi, pA0[r]);
+                  pA1[r] = __fmaf_rn(__low2float(wa1), xa_lo, pA1[r]);
+                  pA1[r] = __fmaf_rn(__high2float(wa1), xa_hi, pA1[r]);
+                  pB0[r] = __fmaf_rn(__low2float(wb0), xb_lo, pB0[r]);
+                  pB0[r] = __fmaf_rn(__high2float(wb0), xb_hi, pB0[r]);
+                  pB1[r] = __fmaf_rn(__low2float(wb1), xb_lo, pB1[r]);
+                  pB1[r] = __fmaf_rn(__high2float(wb1), xb_hi, pB1[r]);
+                }
+              }
+              continue;
+            }
+            const uint4 xa = *reinterpret_cast<const uint4*>(xp);
+            const uint4 xb = *reinterpret_cast<const uint4*>(xp + 512);
+            const uint32_t* va = reinterpret_cast<const uint32_t*>(&xa);
+            const uint32_t* vb = reinterpret_cast<const uint32_t*>(&xb);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              pA0[r] = fma2_f16(a0[i], va[i], pA0[r]);
+              pA1[r] = fma2_f16(a1[i], va[i], pA1[r]);
+              pB0[r] = fma2_f16(b0[i], vb[i], pB0[r]);
+              pB1[r] = fma2_f16(b1[i], vb[i], pB1[r]);
+            }
+          }
         }
 #pragma unroll
         for (int r = 0; r < T; ++r) {
-          if (X32) {
-            // fp32 rows: the same chunks at twice the offsets, plain fp32 fma (exact products)
-            const uint32_t xp = xs_a + r * xrs + 2 * (s * 1024 + tc * 128);
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {  // four values of each group at a time
-              const float4 xa = lds128f(xp + 16 * hf);
-              const float4 xb = lds128f(xp + 1024 + 16 * hf);
-#pragma unroll
-              for (int ii = 0; ii < 2; ++ii) {
-                const int i = 2 * hf + ii;
-                const float xa_lo = ii ? xa.z : xa.x, xa_hi = ii ? xa.w : xa.y;
-                const float xb_lo = ii ? xb.z : xb.x, xb_hi = ii ? xb.w : xb.y;
-#pragma unroll
-                for (int c = 0; c < COLS; ++c) {
-                  const __half2 wa = *reinterpret_cast<const __half2*>(&a[c][i]);
-                  const __half2 wb = *reinterpret_cast<const __half2*>(&b[c][i]);
-                  pA[c][r] = __fmaf_rn(__low2float(wa), xa_lo, pA[c][r]);
-                  pA[c][r] = __fmaf_rn(__high2float(wa), xa_hi, pA[c][r]);
-                  pB[c][r] = __fmaf_rn(__low2float(wb), xb_lo, pB[c][r]);
-                  pB[c][r] = __fmaf_rn(__high2float(wb), xb_hi, pB[c][r]);
-                }
-              }
-            }
-            continue;
-          }
-          // xoff(row, 16s + j (+ 8), tc) = row*GB*512 + s*1024 (+ 512) + tc*128 + j*16
-          const uint32_t xp = xs_a + r * xrs + s * 1024 + tc * 128;
-          const uint4 xa = lds128(xp);
-          const uint4 xb = lds128(xp + 512);
-          const uint32_t* va = reinterpret_cast<const uint32_t*>(&xa);
-          const uint32_t* vb = reinterpret_cast<const uint32_t*>(&xb);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-#pragma unroll
-            for (int c = 0; c < COLS; ++c) {
-              pA[c][r] = fma2_f16(a[c][i], va[i], pA[c][r]);
-              pB[c][r] = fma2_f16(b[c][i], vb[i], pB[c][r]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < T; ++r) {
-        const float mA = lds32f(xm_a + r * xms + 4 * s * GPS), mB = lds32f(xm_a + r * xms + 4 * (s * GPS + 8));
-#pragma unroll
-        for (int c = 0; c < COLS; ++c) {
-          if (KIND == TFX_ACT_E4M3) {
-            acc[c][r] = __fmaf_rn(pA[c][r], __fmul_rn(sA[c], mA), acc[c][r]);
-            acc[c][r] = __fmaf_rn(pB[c][r], __fmul_rn(sB[c], mB), acc[c][r]);
-          } else {
-            float qA = pA[c][r], qB = pB[c][r];
-            const uint16_t* xrow = xraw + (size_t)prow[r] * pj.K;
-            if (!X32 && mA == 0.0f) qA = chain_bf16_exact(cA[c], xrow, gA);
-            else qA = __fmul_rn(qA, mA);
-            if (!X32 && mB == 0.0f) qB = chain_bf16_exact(cB[c], xrow, gB);
-            else qB = __fmul_rn(qB, mB);
-            acc[c][r] = __fmaf_rn(qA, sA[c], acc[c][r]);
-            acc[c][r] = __fmaf_rn(qB, sB[c], acc[c][r]);
-          }
+          fold(r, j, pA0[r], pA1[r], sA0, sA1, cA0, cA1, xm, s * GPS + j);
+          fold(r, j + 8, pB0[r], pB1[r], sB0, sB1, cB0, cB1, xm, s * GPS + 8 + j);
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&B.empty[slot]);
   }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&B.xempty[bx]);  // this warp is done with the activation buffer
   // eight-way tree: ((a0+a4)+(a2+a6)) + ((a1+a5)+(a3+a7)) across the octet
-  float v[COLS][T];
+  float v0r[T], v1r[T];
 #pragma unroll
-  for (int r = 0; r < T; ++r)
-#pragma unroll
-    for (int c = 0; c < COLS; ++c) {
-      float t = acc[c][r];
-      t = t + __shfl_xor_sync(0xffffffffu, t, 4);
-      t = t + __shfl_xor_sync(0xffffffffu, t, 2);
-      t = t + __shfl_xor_sync(0xffffffffu, t, 1);
-      v[c][r] = t;
-    }
+  for (int r = 0; r < T; ++r) {
+    float v0 = acc0[r], v1 = acc1[r];
+    v0 = v0 + __shfl_xor_sync(0xffffffffu, v0, 4);
+    v1 = v1 + __shfl_xor_sync(0xffffffffu, v1, 4);
+    v0 = v0 + __shfl_xor_sync(0xffffffffu, v0, 2);
+    v1 = v1 + __shfl_xor_sync(0xffffffffu, v1, 2);
+    v0 = v0 + __shfl_xor_sync(0xffffffffu, v0, 1);
+    v1 = v1 + __shfl_xor_sync(0xffffffffu, v1, 1);
+    v0r[r] = v0;
+    v1r[r] = v1;
+  }
   if (ewait) warp_wait(&B.eempty[be], eph, P, abort_flag, dead);
   if (!dead && j == 0) {
 #pragma unroll
     for (int r = 0; r < T; ++r)
       if (r < real) {
-#pragma unroll
-        for (int c = 0; c < COLS; ++c) epi[r * 64 + col[c]] = v[c][r];
+        epi[r * 64 * UPI + 64 * uu + rr] = v0r[r];
+        epi[r * 64 * UPI + 64 * uu + 32 + rr] = v1r[r];
       }
   }
   __syncwarp();
   if (lane == 0) mbar_arrive(&B.efull[be]);
 }
 
-template <int KIND, int MAXR, bool DOWN, int COLS>
-__device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const Proj& pj, uint8_t* ring,
-                                              const Bars& B, int bx, int be, uint32_t eph, bool ewait,
-                                              volatile int* abort_flag, const uint8_t* xs_s, const float* xm_s,
-                                              const int* prow, const uint16_t* xraw, int real, uint32_t& it,
-                                              bool& dead, float* epi) {
+template <int KIND, int MAXR, bool DOWN, int UPI>
+__device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const Proj& pj, const uint8_t* smem,
+                                              const Layout& Ly, const Bars& B, int be, uint32_t eph, bool ewait,
+                                              volatile int* abort_flag, const int* r_prow, int pos, int real,
+                                              uint32_t& it, bool& dead, float* epi) {
   constexpr int LIM = DOWN ? (MAXR < MAX_PASS_D ? MAXR : MAX_PASS_D) : MAXR;
-#define TFX_PASS(TT)                                                                                          \
-  if constexpr (TT <= LIM)                                                                                    \
-    run_pass<KIND, TT, COLS, DOWN && KIND == TFX_ACT_BF16>(P, pj, ring, B, bx, be, eph, ewait, abort_flag, xs_s, \
-                                                           xm_s, prow, xraw, real, it, dead, epi)
+  constexpr bool X32 = DOWN && KIND == TFX_ACT_BF16;
+#define TFX_PASS(TT)                                                                                         \
+  if constexpr (TT <= LIM)                                                                                   \
+    run_pass<KIND, TT, UPI, X32, (TT > 4)>(P, pj, smem, Ly, B, be, eph, ewait, abort_flag, r_prow, pos, real, \
+                                           DOWN, it, dead, epi)
   switch (t) {
     case 1: TFX_PASS(1); break;
     case 2: TFX_PASS(2); break;
@@ -740,41 +841,55 @@ __device__ __forceinline__ void dispatch_pass(int t, const RowsParams& P, const 
 #undef TFX_PASS
 }
 
-// One pass as the helper sees it (all fields warp-uniform).
+// One pass as the epilogue warp sees it (all fields warp-uniform).
 struct HPass {
   bool dn, last;
-  int a, u, real, pidx;
+  int a, ub, nu, real, pidx;  // ub: first packed unit of the item, nu: its units
   int pair[8];
 };
 
-// Epilogue warp: the epilogue of one pass, from result buffer epi. Gate/up: SwiGLU, the
+// Epilogue warp: the epilogue of one pass, from result buffer epi; the pass's (row, unit)
+// items are taken four at a time, so that their latency chains overlap. Gate/up: SwiGLU, the
 // activation quantiser and h (+ debug copies); fused launches publish a finished gate/up unit.
-// Down: the expert outputs d; fused launches combine each (row, block) whose last slot this
-// writes.
-template <int KIND, int PH>
+// Down: the expert outputs d; fused launches then count each (row, 64-output block) written,
+// with one fence for the whole pass, and combine the blocks whose last slot this pass wrote.
+template <int KIND, int PH, int UPI>
 __device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars& B, const float* epi,
                                 const int* r_prow, const int* r_pslot, const int* r_rowcnt, int32_t* done_upc,
                                 int32_t* slots_done, volatile int* abort_flag, bool& dead) {
   const int lane = threadIdx.x & 31;
   const int be = q.pidx & 1;
   warp_wait(&B.efull[be], (q.pidx >> 1) & 1, P, abort_flag, dead);
-  if (!dead) {
-    for (int r = 0; r < q.real; ++r) {
-      const int p = q.pair[r];
-      if (!q.dn) {
-        const int I = P.I;
-        const int nn = 32 * q.u + lane;
-        const float g = epi[r * 64 + lane], uu = epi[r * 64 + 32 + lane];
-        const float den = __fadd_rn(1.0f, expf(-g));
-        const float hv = __fmul_rn(__fdiv_rn(g, den), uu);
+  const int n_items = q.real * q.nu;  // item i: row i / nu, unit i % nu
+  if (!dead && !q.dn) {
+    const int I = P.I;
+    for (int i0 = 0; i0 < n_items; i0 += 4) {
+      float g[4], u[4], hv[4];
+      int pp[4], nn[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (i0 + c >= n_items) break;
+        const int i = i0 + c, r = i / q.nu, uu = i - r * q.nu;
+        const float* er = epi + r * 64 * UPI + 64 * uu;
+        pp[c] = q.pair[r];
+        nn[c] = 32 * (q.ub + uu) + lane;
+        g[c] = er[lane];
+        u[c] = er[32 + lane];
+        const float den = __fadd_rn(1.0f, expf(-g[c]));
+        hv[c] = __fmul_rn(__fdiv_rn(g[c], den), u[c]);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (i0 + c >= n_items) break;
+        const size_t p = (size_t)pp[c];
         if (P.gu_dbg) {
-          P.gu_dbg[(size_t)p * 2 * I + nn] = g;
-          P.gu_dbg[(size_t)p * 2 * I + I + nn] = uu;
+          P.gu_dbg[p * 2 * I + nn[c]] = g[c];
+          P.gu_dbg[p * 2 * I + I + nn[c]] = u[c];
         }
-        if (P.h_dbg) P.h_dbg[(size_t)p * I + nn] = hv;
+        if (P.h_dbg) P.h_dbg[p * I + nn[c]] = hv[c];
         if (KIND == TFX_ACT_E4M3) {
-          const bool bad = __any_sync(0xffffffffu, isnan(hv) || isinf(hv));
-          const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
+          const bool bad = __any_sync(0xffffffffu, isnan(hv[c]) || isinf(hv[c]));
+          const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));
           uint32_t sc;
           if (bad) sc = 255u;
           else if (amax_b == 0u) sc = 127u;
@@ -782,40 +897,62 @@ __device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars&
             const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
             sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
           }
-          const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv, e8m0_recip_f32(sc)));
-          static_cast<uint8_t*>(P.h)[(size_t)p * I + nn] = (uint8_t)code;
-          if (lane == 0) P.hs[(size_t)p * (I / 32) + q.u] = (uint8_t)sc;
+          const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv[c], e8m0_recip_f32(sc)));
+          static_cast<uint8_t*>(P.h)[p * I + nn[c]] = (uint8_t)code;
+          if (lane == 0) P.hs[p * (I / 32) + (nn[c] >> 5)] = (uint8_t)sc;
         } else {
-          static_cast<__nv_bfloat16*>(P.h)[(size_t)p * I + nn] = __float2bfloat16_rn(hv);
+          static_cast<__nv_bfloat16*>(P.h)[p * I + nn[c]] = __float2bfloat16_rn(hv[c]);
         }
+      }
+    }
+  } else if (!dead) {
+    bool bad = false;
+    for (int i = 0; i < n_items; ++i) {
+      const int r = i / q.nu, uu = i - r * q.nu;
+      const int p = q.pair[r], row = r_prow[p], slot = r_pslot[p];
+      if (row >= 0 && row < P.R && slot >= 0 && slot < P.k) {
+        const float* er = epi + r * 64 * UPI + 64 * uu;
+        float* dst = P.out + ((size_t)row * P.k + slot) * P.H + 64 * (q.ub + uu);
+        dst[lane] = er[lane];
+        dst[32 + lane] = er[32 + lane];
       } else {
-        const int row = r_prow[p], slot = r_pslot[p];
+        bad = true;
+      }
+    }
+    if (bad && lane == 0) report(P.status, TFX_ST_SHAPE);
+    if (PH == PH_FUSED) {
+      // combine (row, block) in the CTA that writes the row's last slot
+      __threadfence();
+      __syncwarp();
+      int last = 0, ctr = -1, row = -1, blk = 0;
+      if (lane < n_items) {
+        const int r = lane / q.nu, uu = lane - r * q.nu;
+        const int p = q.pair[r];
+        row = r_prow[p];
+        const int slot = r_pslot[p];
+        blk = q.ub + uu;
         if (row >= 0 && row < P.R && slot >= 0 && slot < P.k) {
-          float* dst = P.out + ((size_t)row * P.k + slot) * P.H + 64 * q.u;
-          dst[lane] = epi[r * 64 + lane];
-          dst[32 + lane] = epi[r * 64 + 32 + lane];
-          if (PH == PH_FUSED) {
-            // combine (row, block u) in the CTA that writes the row's last slot
-            __threadfence();
-            int last = 0;
-            if (lane == 0) last = atomicAdd(&slots_done[(size_t)row * P.pd.units + q.u], 1) == r_rowcnt[row] - 1;
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-              if (lane == 0) slots_done[(size_t)row * P.pd.units + q.u] = 0;  // last user of the counter
-              __threadfence();
+          ctr = row * P.pd.units + blk;
+          last = atomicAdd(&slots_done[ctr], 1) == r_rowcnt[row] - 1;
+          if (last) slots_done[ctr] = 0;  // last user of the counter
+        }
+      }
+      unsigned lm = __ballot_sync(0xffffffffu, last);
+      if (lm) {
+        __threadfence();
+        while (lm) {
+          const int src = __ffs(lm) - 1;
+          lm &= lm - 1;
+          const int rw = __shfl_sync(0xffffffffu, row, src), bk = __shfl_sync(0xffffffffu, blk, src);
 #pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int m = 64 * q.u + 32 * hh + lane;
-                float yv = 0.0f;
-                for (int jj = 0; jj < P.k; ++jj)
-                  yv = __fmaf_rn(P.topk_w[(size_t)row * P.k + jj], __ldcg(P.out + ((size_t)row * P.k + jj) * P.H + m), yv);
-                P.y[(size_t)row * P.H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
-                if (P.y32) P.y32[(size_t)row * P.H + m] = yv;
-              }
-            }
+          for (int hh = 0; hh < 2; ++hh) {
+            const int m = 64 * bk + 32 * hh + lane;
+            float yv = 0.0f;
+            for (int jj = 0; jj < P.k; ++jj)
+              yv = __fmaf_rn(P.topk_w[(size_t)rw * P.k + jj], __ldcg(P.out + ((size_t)rw * P.k + jj) * P.H + m), yv);
+            P.y[(size_t)rw * P.H + m] = __bfloat16_as_ushort(__float2bfloat16_rn(yv));
+            if (P.y32) P.y32[(size_t)rw * P.H + m] = yv;
           }
-        } else if (lane == 0) {
-          report(P.status, TFX_ST_SHAPE);
         }
       }
     }
@@ -831,9 +968,10 @@ __device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars&
 
 // ---------------------------------------------------------------- the sequence of passes
 // Every role walks the same sequence of passes. Separate launches: this CTA's items
-// (blockIdx.x + i * gridDim.x; an item is (active expert, output block), its passes sized by
-// the rows left). Fused launch: the claimed work units, each one pass: unit i < n_upc is
-// gate/up pass list entry i / units, output block i % units; the down units follow.
+// (blockIdx.x + i * gridDim.x; an item is (active expert, UPI packed units of outputs), its
+// passes sized by the rows left). Fused launch: the claimed work units, each one pass: unit
+// i < n_upc is gate/up pass list entry i / items, item i % items (items = units of an expert
+// in groups of UPI); the down units follow.
 struct PassDesc {
   bool dn, first, last;
   int a, u, e, p0, pos, real, t, pidx;
@@ -850,7 +988,7 @@ struct SeqCtx {
   const int *plist_u, *plist_d;  // fused: pass lists
 };
 // next_item() yields this CTA's next item (or unit) index, or -1 when there is none.
-template <int PH, typename NextItem>
+template <int PH, int UPI, typename NextItem>
 __device__ __forceinline__ bool gen_next(PassGen& g, PassDesc& d, const RowsParams& P, const SeqCtx& c,
                                          NextItem&& next_item) {
   if constexpr (PH == PH_FUSED) {
@@ -864,7 +1002,8 @@ __device__ __forceinline__ bool gen_next(PassGen& g, PassDesc& d, const RowsPara
       const bool dn = i >= c.n_upc;
       const Proj& pj = dn ? P.pd : P.pu;
       const int li = dn ? i - c.n_upc : i;
-      const int q = li / pj.units, u = li - q * pj.units;
+      const int items = (pj.units + UPI - 1) / UPI;
+      const int q = li / items, u = li - q * items;
       const int ent = (dn ? c.plist_d : c.plist_u)[q];
       const int a = ent & 1023, start = (ent >> 10) & 255, real = (ent >> 18) & 15, t = (ent >> 22) & 15;
       const int e = c.act[a];
@@ -900,7 +1039,8 @@ __device__ __forceinline__ bool gen_next(PassGen& g, PassDesc& d, const RowsPara
       const bool dn = g.item >= c.n_upc;
       const Proj& pj = dn ? P.pd : P.pu;
       const int li = dn ? g.item - c.n_upc : g.item;
-      const int a = li / pj.units, u = li - a * pj.units;
+      const int items = (pj.units + UPI - 1) / UPI;
+      const int a = li / items, u = li - a * items;
       const int e = c.act[a];
       const int p0 = (e >= 0 && e < P.E) ? c.offs[e] : 0;
       const int n = (e >= 0 && e < P.E) ? c.offs[e + 1] - p0 : 0;
@@ -939,10 +1079,10 @@ __device__ __forceinline__ bool gen_next(PassGen& g, PassDesc& d, const RowsPara
 }
 
 // ---------------------------------------------------------------- the kernel
-// Roles: the consumer warps compute; the next warp produces (weight stages); the next stages:
-// it brings each pass's activation rows in by bulk copy one pass ahead and converts them into
-// the f16 buffer; the last runs each pass's epilogue (SwiGLU and quantisation of h, or the d
-// rows and, in the fused launch, the combine) while the consumers go on with the next pass.
+// Roles: the consumer warps compute; the next warp produces (weight stages and the pass's
+// activation rows of each stage, by bulk copy); the next converts each stage's activations in
+// its slot and completes the slot; the last runs each pass's epilogue (SwiGLU and quantisation
+// of h, or the d rows and, in the fused launch, the combine) while the consumers go on.
 template <int KIND, int MAXR_U, int MAXR_D, int PH>
 struct RowsShape {
   static constexpr int MAXR = ((PH & PH_UPC) && MAXR_U > MAXR_D) || !(PH & PH_DOWN) ? MAXR_U : MAXR_D;
@@ -950,48 +1090,45 @@ struct RowsShape {
 };
 
 template <int KIND, int MAXR_U, int MAXR_D, int PH>
-__global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
-    __maxnreg__((RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::MAXREG)) rows_kernel(const RowsParams P) {
+__global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
+                                  RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::MINB)
+    rows_kernel(const RowsParams P) {
   using Sh = RowsShape<KIND, MAXR_U, MAXR_D, PH>;
   using C = typename Sh::C;
+  using SR = SlotRow<KIND>;
   constexpr int MAXR = Sh::MAXR;
-  constexpr int NCW = C::NCW, NT = C::NT;
+  constexpr int NCW = C::NCW, NT = C::NT, UPI = C::UPI;
   constexpr int AB = KIND == TFX_ACT_E4M3 ? 1 : 2;  // activation bytes per element
   extern __shared__ __align__(128) uint8_t smem[];
-  const Layout Ly = layout_of(P, MAXR);
+  const Layout Ly = layout_of(P, MAXR, UPI, SR::ACT);
   Bars B;
   B.full = reinterpret_cast<uint64_t*>(smem + Ly.bars);
   B.empty = B.full + MAX_NSTAGE;
-  B.xfull = B.empty + MAX_NSTAGE;
-  B.xempty = B.xfull + 2;
-  B.efull = B.xempty + 2;
+  B.efull = B.empty + MAX_NSTAGE;
   B.eempty = B.efull + 2;
-  uint64_t* rawfull = B.eempty + 2;
-  uint64_t* qfull = rawfull + 1;  // fused: claimed-item queue, producer -> helper and consumers
-  uint64_t* qempty = qfull + QD;  //        and back
+  uint64_t* qfull = B.eempty + 2;  // fused: claimed-item queue, producer -> stager, epilogue, consumers
+  uint64_t* qempty = qfull + QD;   //        and back
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.ctrl);
-  int* pdesc = reinterpret_cast<int*>(smem + Ly.pdesc);  // [2][16]: prow[8], ppair[8]
-  float* epi = reinterpret_cast<float*>(smem + Ly.epi);    // [2][8][64]
+  int* qid = reinterpret_cast<int*>(smem + Ly.ctrl + 16);    // [QD] claimed item ids
+  float* epi = reinterpret_cast<float*>(smem + Ly.epi);      // [2][maxr][64 upi]
   uint8_t* ring = smem + Ly.ring;
-  uint8_t* raw = smem + Ly.raw;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int NST = P.nstage, NXB = P.nxb;
+  const int NST = P.nstage;
+  // the consumers' weight-scale table (1 KB) is brought into L1 while the row lists are built
+  if (tid < (int)sizeof(E8m0Table) / 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(e8m0_table.v + 32 * tid));
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(&B.full[s], 1);
+      mbar_init(&B.full[s], 2);  // the producer's weights (with their bytes) and the stager
       mbar_init(&B.empty[s], NCW);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&B.xfull[b], 1);
-      mbar_init(&B.xempty[b], NCW);
       mbar_init(&B.efull[b], NCW);
       mbar_init(&B.eempty[b], 1);
     }
-    mbar_init(rawfull, 1);
     for (int b = 0; b < QD; ++b) {
       mbar_init(&qfull[b], 1);
-      mbar_init(&qempty[b], NCW + 2);
+      mbar_init(&qempty[b], NCW + 1 + C::NSTG);
     }
     mbar_fence_init();
     *abort_flag = 0;
@@ -1002,6 +1139,7 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
   const uint16_t *np_u = nullptr, *np_d = nullptr;  // fused: passes per active expert
   int n_act;
   SeqCtx sc;
+  const int items_u = (P.pu.units + UPI - 1) / UPI, items_d = (P.pd.units + UPI - 1) / UPI;
   if (PH == PH_FUSED) {
     SRoute rt;
     route_smem<NT>(P, reinterpret_cast<int*>(smem + Ly.route), rt, tid);  // synchronises the block
@@ -1015,8 +1153,8 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
     r_rowcnt = rt.rowcnt;
     sc.plist_u = rt.plist_u;
     sc.plist_d = rt.plist_d;
-    sc.n_upc = rt.nlist[0] * P.pu.units;
-    sc.total = sc.n_upc + rt.nlist[1] * P.pd.units;
+    sc.n_upc = rt.nlist[0] * items_u;
+    sc.total = sc.n_upc + rt.nlist[1] * items_d;
     if (blockIdx.x == 0) {  // publish the row lists
       const int Pn = P.R * P.k;
       for (int i = tid; i <= P.E; i += NT) P.offs[i] = rt.offs[i];
@@ -1035,8 +1173,8 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
     r_pslot = P.pair_slot;
     r_act = P.active;
     sc.plist_u = sc.plist_d = nullptr;
-    sc.n_upc = (PH & PH_UPC) ? n_act * P.pu.units : 0;
-    sc.total = sc.n_upc + ((PH & PH_DOWN) ? n_act * P.pd.units : 0);
+    sc.n_upc = (PH & PH_UPC) ? n_act * items_u : 0;
+    sc.total = sc.n_upc + ((PH & PH_DOWN) ? n_act * items_d : 0);
   }
   sc.act = r_act;
   sc.offs = r_offs;
@@ -1044,16 +1182,22 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
   int32_t* done_upc = PH == PH_FUSED ? P.scratch + 2 : nullptr;
   int32_t* down_seen = PH == PH_FUSED ? P.scratch + 2 + P.E : nullptr;
   int32_t* slots_done = PH == PH_FUSED ? P.scratch + 2 + 2 * P.E : nullptr;
-  int* qid = reinterpret_cast<int*>(smem + Ly.ctrl + 16);  // [QD] claimed item ids
   PassGen gen = {};
   PassDesc d;
+  // rows of a pass: token rows (gate/up) or pair rows (down); padding repeats the last
+  auto row_of = [&](const PassDesc& q, int r) {
+    const int src = q.pos + min(r, q.real - 1);
+    if (q.dn) return src;
+    const int row = r_prow[src];
+    return (row < 0 || row >= P.R) ? 0 : row;
+  };
   // Separate launches stride over the items; the fused launch hands units out dynamically: the
   // producer claims them from a global counter, in order (gate/up units pass-major, then down
-  // units), and passes them to the helper and the consumers through a small queue.
+  // units), and passes them to the other roles through a small queue.
   int static_next = blockIdx.x - (int)gridDim.x;
   uint32_t qpos = 0;
   auto next_static = [&]() { static_next += gridDim.x; return static_next; };
-  auto next_popped = [&]() {  // helper and consumers (warp-wide)
+  auto next_popped = [&]() {  // stager, epilogue and consumers (warp-wide)
     const int slot = qpos % QD;
     bool dq = false;
     warp_wait(&qfull[slot], (qpos / QD) & 1, P, abort_flag, dq);
@@ -1096,9 +1240,9 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
         ++claims;
         return v;
       };
-      // The queue runs one unit ahead of the producer, so the stager learns of the next unit
-      // (and can stage its activations) while the current one streams. The claim of that next
-      // unit is made once the current unit's first stages are on their way.
+      // The queue runs one unit ahead of the producer, so the other roles learn of the next
+      // unit while the current one streams. The claim of that next unit is made once the
+      // current unit's first stages are on their way.
       int ahead = -2;
       bool pending = false;
       auto claim_pending = [&]() {
@@ -1116,9 +1260,10 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
         return v;
       };
       auto next_prod = [&]() { return PH == PH_FUSED ? next_claimed() : next_static(); };
-      while (!stop && gen_next<PH>(gen, d, P, sc, next_prod)) {
+      while (!stop && gen_next<PH, UPI>(gen, d, P, sc, next_prod)) {
         const Proj& pj = d.dn ? P.pd : P.pu;
-        const uint8_t* src = pj.w + (size_t)d.e * pj.expert_bytes + (size_t)d.u * pj.unit_bytes;
+        const int ub = UPI * d.u, nu = min(UPI, pj.units - ub);
+        const uint8_t* src = pj.w + (size_t)d.e * pj.expert_bytes + (size_t)ub * pj.unit_bytes;
         for (int s = 0; s < pj.S; ++s, ++it) {
           const int slot = it % NST;
           const uint32_t ph = (it / NST) & 1u;
@@ -1130,14 +1275,16 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
             break;
           }
           if (*abort_flag) { stop = true; break; }
-          mbar_arrive_expect_tx(&B.full[slot], STAGE_B);
-          bulk_g2s(ring + (size_t)slot * STAGE_B, src + (size_t)s * STAGE_B, STAGE_B, &B.full[slot]);
+          uint8_t* sb = ring + (size_t)slot * Ly.slot;
+          mbar_arrive_expect_tx(&B.full[slot], (uint32_t)(nu * STAGE_B));
+          for (int v = 0; v < nu; ++v)
+            bulk_g2s(sb + v * STAGE_B, src + (size_t)v * pj.unit_bytes + (size_t)s * STAGE_B, STAGE_B, &B.full[slot]);
           if (PH == PH_FUSED && (it + 1 >= (uint32_t)NST || s == pj.S - 1)) claim_pending();
         }
       }
       if (PH == PH_FUSED) claim_pending();
       if (PH == PH_FUSED && !gen.done) {
-        // stopped early (abort): tell the helper and the consumers there is nothing more
+        // stopped early (abort): tell the other roles there is nothing more
         *abort_flag = 1;
         for (int q = 0; q < 2 * QD && !gen.done; ++q) {
           const int slot = claims % QD;
@@ -1147,7 +1294,8 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
           ++claims;
         }
       }
-      // Drain: every issued stage must have landed before the block may exit.
+      // Drain: every issued stage must have landed before the block may exit (the slot's phase
+      // also needs the stager, which completes it unless the block aborted).
       const uint32_t first = it > (uint32_t)NST ? it - NST : 0u;
       for (uint32_t q = first; q < it; ++q) {
         if (!mbar_wait(&B.full[q % NST], (q / NST) & 1u, P.timeout_ns)) {
@@ -1156,158 +1304,84 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
         }
       }
     }
-  } else if (warp == C::W_HELP) {
-    // ---------------------------------------------------------------- helper
+  } else if (warp >= C::W_HELP && warp < C::W_HELP + C::NSTG) {
+    // ---------------------------------------------------------------- stagers
+    // Stager sid converts the stages whose running index is sid modulo NSTG, so that one
+    // stage's loads are in flight while another converts.
+    const int sid = warp - C::W_HELP;
     bool dead = false;
-    uint32_t raw_issued = 0, raw_waited = 0;
 
-    // rows of a pass: token rows (gate/up) or pair rows (down); padding repeats the last
-    auto row_of = [&](const PassDesc& q, int r) {
-      const int src = q.pos + min(r, q.real - 1);
-      if (q.dn) return src;
-      const int row = r_prow[src];
-      return (row < 0 || row >= P.R) ? 0 : row;
-    };
-    // fused down: wait (bounded) until every gate/up unit of the expert has published its h
-    auto wait_dependency = [&](const PassDesc& q) {
-      if (!(PH == PH_FUSED && q.dn && q.first) || dead) return;
-      int okw = 1;
-      if (lane == 0) {
-        const int need = np_u[q.a] * P.pu.units;
-        const uint64_t t0 = global_ns();
-        while (true) {
-          int v;
-          asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(done_upc + q.a) : "memory");
-          if (v >= need) break;
-          if (*abort_flag || global_ns() - t0 > P.timeout_ns) {
-            if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
-            *abort_flag = 1;
-            okw = 0;
-            break;
-          }
-          __nanosleep(64);
-        }
-        asm volatile("fence.proxy.async.global;" ::: "memory");  // h is read next by the async proxy
-        // the expert's last down unit past this point returns both counters to zero
-        if (okw && atomicAdd(down_seen + q.a, 1) == np_d[q.a] * P.pd.units - 1) {
-          done_upc[q.a] = 0;
-          down_seen[q.a] = 0;
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, okw, 0)) dead = true;
-    };
-    // bulk copies of the pass's activation rows (and scales) into the raw buffer
-    // Rows of the pass last staged into each activation buffer (lane r < 8 holds row r): a pass
-    // whose buffer already holds its rows (every gate/up pass of a one-row launch, for one) is
-    // not staged again.
-    int krow0 = -1, krow1 = -1, kdn0 = -1, kdn1 = -1, kreal0 = 0, kreal1 = 0;
-    bool pend_skip = false, pend_copy = false;
-    // other: compare with the buffer the pass does not use (two buffers)
-    auto same_rows = [&](const PassDesc& q, bool other = false) {
-      const bool b1 = NXB == 2 && (((q.pidx & 1) != 0) != other);
-      const int mine = lane < 8 ? row_of(q, lane) : 0;
-      const bool eq = lane >= 8 || (b1 ? krow1 : krow0) == mine;
-      return (b1 ? kdn1 : kdn0) == (int)q.dn && (b1 ? kreal1 : kreal0) == q.t && __all_sync(0xffffffffu, eq);
-    };
-    auto issue_raw = [&](const PassDesc& q) {
-      pend_skip = same_rows(q);
-      pend_copy = !pend_skip && NXB == 2 && same_rows(q, true);  // the other buffer has them: copy it
-      if (pend_skip || pend_copy || !P.use_raw || dead) return;
-      const Proj& pj = q.dn ? P.pd : P.pu;
-      const int rowb = pj.K * AB;
-      const bool tsc = KIND == TFX_ACT_E4M3 && (q.dn ? P.sc_tma_d : P.sc_tma_u);
-      const uint8_t* X8 = q.dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
-      const uint8_t* XS = q.dn ? P.hs : P.xs;
-      int rows[8];
+    uint32_t it = 0;
+    auto next_h = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
+    while (gen_next<PH, UPI>(gen, d, P, sc, next_h)) {
+      const Proj& pj = d.dn ? P.pd : P.pu;
+      const uint8_t* X8 = d.dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
+      const uint8_t* XS = d.dn ? P.hs : P.xs;
+      int rw[MAXR];  // the pass's rows (padding rows repeat the last real row)
 #pragma unroll
-      for (int r = 0; r < 8; ++r) rows[r] = row_of(q, r);
-      __syncwarp();  // the previous conversion's reads of the raw buffer are done
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(rawfull, (uint32_t)(q.t * (rowb + (tsc ? pj.G : 0))));
-        for (int r = 0; r < q.t; ++r) {
-          bulk_g2s(raw + r * P.raw_row, X8 + (size_t)rows[r] * rowb, rowb, rawfull);
-          if (tsc) bulk_g2s(raw + MAXR * P.raw_row + r * P.raw_sc, XS + (size_t)rows[r] * pj.G, pj.G, rawfull);
+      for (int r = 0; r < MAXR; ++r) rw[r] = row_of(d, min(r, d.t - 1));
+      if (PH == PH_FUSED && d.dn && d.first && !dead) {
+        // fused down: wait (bounded) until every gate/up unit of the expert has published its h
+        int okw = 1;
+        if (lane == 0) {
+          const int need = np_u[d.a] * items_u;
+          const uint64_t t0 = global_ns();
+          while (true) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(done_upc + d.a) : "memory");
+            if (v >= need) break;
+            if (*abort_flag || global_ns() - t0 > P.timeout_ns) {
+              if (*abort_flag == 0) report(P.status, TFX_ST_TIMEOUT);
+              *abort_flag = 1;
+              okw = 0;
+              break;
+            }
+            __nanosleep(64);
+          }
+          // every stager of every down unit of the expert counts itself past this wait; the last
+          // one returns both counters to zero (no waiter can still be reading them then)
+          if (okw && atomicAdd(down_seen + d.a, 1) == C::NSTG * np_d[d.a] * items_d - 1) {
+            done_upc[d.a] = 0;
+            down_seen[d.a] = 0;
+          }
         }
-      }
-      ++raw_issued;
-    };
-    // wait for the pass's activation buffer, fill it, hand it to the consumers
-    auto finish_stage = [&](const PassDesc& q) {
-      const Proj& pj = q.dn ? P.pd : P.pu;
-      const int bx = NXB == 2 ? (q.pidx & 1) : 0;
-      if (q.pidx >= NXB) warp_wait(&B.xempty[bx], ((q.pidx / NXB) & 1) ^ 1, P, abort_flag, dead);
-      int* pd = pdesc + 16 * bx;
-      if (lane < 8) {
-        pd[lane] = row_of(q, lane);
-        pd[8 + lane] = q.pos + min(lane, q.real - 1);
-      }
-      __syncwarp();
-      uint8_t* xs_s = smem + Ly.xs + bx * Ly.xs_stride;
-      float* xm_s = reinterpret_cast<float*>(smem + Ly.xm + bx * Ly.xm_stride);
-      const uint8_t* X8 = q.dn ? static_cast<const uint8_t*>(P.h) : static_cast<const uint8_t*>(P.x);
-      const uint8_t* XS = q.dn ? P.hs : P.xs;
-      if (pend_skip) {
-        // the buffer holds these rows already
-      } else if (pend_copy) {
-        if (!dead) {  // the other buffer holds these rows, staged the same way: copy its rows and multipliers
-          const int xb = (KIND == TFX_ACT_BF16 && q.dn ? 2 : 1) * q.t * pj.GB * 512;
-          const uint4* s4 = reinterpret_cast<const uint4*>(smem + Ly.xs + (bx ^ 1) * Ly.xs_stride);
-          uint4* d4 = reinterpret_cast<uint4*>(xs_s);
-          for (int i = lane; i < xb / 16; i += kWarp) d4[i] = s4[i];
-          const float* sm = reinterpret_cast<const float*>(smem + Ly.xm + (bx ^ 1) * Ly.xm_stride);
-          for (int i = lane; i < q.t * pj.GB * 8; i += kWarp) xm_s[i] = sm[i];
-        }
-      } else if (P.use_raw) {
-        if (raw_waited < raw_issued) {
-          warp_wait(rawfull, raw_waited & 1u, P, abort_flag, dead);
-          ++raw_waited;
-        }
-        const bool tsc = KIND == TFX_ACT_E4M3 && (q.dn ? P.sc_tma_d : P.sc_tma_u);
-        if (!dead) {
-          if (tsc)
-            stage_rows<KIND, true, true>(raw, P.raw_row, raw + MAXR * P.raw_row, P.raw_sc, pj.K, pj.G, pj.GB, xs_s,
-                                         xm_s, pd, q.t, lane, 32);
-          else if (KIND == TFX_ACT_BF16 && q.dn)
-            stage_rows<KIND, true, false, true>(raw, P.raw_row, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.t,
-                                                lane, 32);
-          else
-            stage_rows<KIND, true, false>(raw, P.raw_row, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.t,
-                                          lane, 32);
-        }
-      } else if (!dead) {
-        if (KIND == TFX_ACT_BF16 && q.dn)
-          stage_rows<KIND, false, false, true>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd,
-                                               q.t, lane, 32);
-        else
-          stage_rows<KIND, false, false>(X8, (size_t)pj.K * AB, XS, pj.G, pj.K, pj.G, pj.GB, xs_s, xm_s, pd, q.t,
-                                         lane, 32);
-      }
-      if (!pend_skip && !dead) {
-        const int mine = lane < 8 ? row_of(q, lane) : 0;
-        if (bx) { krow1 = mine; kdn1 = q.dn; kreal1 = q.t; }
-        else { krow0 = mine; kdn0 = q.dn; kreal0 = q.t; }
+        if (!__shfl_sync(0xffffffffu, okw, 0)) dead = true;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&B.xfull[bx]);
-    };
-    PassDesc cur, nxt;
-    auto next_hc = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
-    bool hc = gen_next<PH>(gen, cur, P, sc, next_hc);
-    if (hc) {
-      wait_dependency(cur);
-      issue_raw(cur);
+      for (int s = 0; s < pj.S; ++s, ++it) {
+        if ((int)(it % C::NSTG) != sid) continue;
+        const int slot = it % NST;
+        const uint32_t ph = (it / NST) & 1u;
+        // the stage's loads are issued first; the slot is free once the consumers have released
+        // its previous use, and only then is it written
+        auto run_stage = [&](auto mode_tag, auto coh_tag, const auto& rows) {
+          constexpr int MODE = decltype(mode_tag)::value;
+          constexpr bool COH = decltype(coh_tag)::value;
+          constexpr int MR = sizeof(rows) / sizeof(int);
+          StageRegs<KIND, MODE, MR> sr;
+          if (!dead) stage_load<KIND, MODE, COH, MR>(sr, X8, XS, d.t, s, pj.K, pj.G, rows, lane);
+          if ((it < (uint32_t)NST || warp_wait(&B.empty[slot], ph ^ 1u, P, abort_flag, dead)) && !dead) {
+            uint8_t* sb = ring + (size_t)slot * Ly.slot;
+            stage_store<KIND, MODE, COH, MR>(sr, sb + Ly.act, SR::ACT, reinterpret_cast<float*>(sb + Ly.xm), GPS, d.t, s,
+                                             pj.K, pj.G, X8, rows, lane);
+          }
+        };
+        if (KIND == TFX_ACT_E4M3) {
+          if (d.dn) run_stage(std::integral_constant<int, 0>(), std::true_type(), rw);
+          else run_stage(std::integral_constant<int, 0>(), std::false_type(), rw);
+        } else if (d.dn) {
+          int rwd[MAXR_D];
+#pragma unroll
+          for (int r = 0; r < MAXR_D; ++r) rwd[r] = rw[r];
+          run_stage(std::integral_constant<int, 2>(), std::true_type(), rwd);
+        } else {
+          run_stage(std::integral_constant<int, 1>(), std::false_type(), rw);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.full[slot]);
+      }
+      __syncwarp();
     }
-    while (hc) {
-      finish_stage(cur);
-      if (!gen_next<PH>(gen, nxt, P, sc, next_hc)) break;
-      wait_dependency(nxt);
-      issue_raw(nxt);
-      cur = nxt;
-    }
-    // a bulk copy issued before an abort must land before the block may exit
-    if (lane == 0 && raw_waited < raw_issued && !mbar_wait(rawfull, raw_waited & 1u, P.timeout_ns))
-      report(P.status, TFX_ST_TIMEOUT);
   } else if (warp == C::W_EPI) {
     // ---------------------------------------------------------------- epilogue
     bool dead = false;
@@ -1316,38 +1390,33 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
       hp.dn = q.dn;
       hp.last = q.last;
       hp.a = q.a;
-      hp.u = q.u;
+      const Proj& pj = q.dn ? P.pd : P.pu;
+      hp.ub = UPI * q.u;
+      hp.nu = min(UPI, pj.units - hp.ub);
       hp.real = q.real;
       hp.pidx = q.pidx;
 #pragma unroll
       for (int r = 0; r < 8; ++r) hp.pair[r] = q.pos + min(r, q.real - 1);
-      helper_epilogue<KIND, PH>(P, hp, B, epi + (q.pidx & 1) * 512, r_prow, r_pslot, r_rowcnt, done_upc, slots_done,
-                                abort_flag, dead);
+      helper_epilogue<KIND, PH, UPI>(P, hp, B, epi + (q.pidx & 1) * (MAXR * 64 * UPI), r_prow, r_pslot, r_rowcnt,
+                                     done_upc, slots_done, abort_flag, dead);
     };
-
     auto next_e = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
     PassDesc q;
-    while (gen_next<PH>(gen, q, P, sc, next_e)) epilogue(q);
+    while (gen_next<PH, UPI>(gen, q, P, sc, next_e)) epilogue(q);
   } else {
     // ---------------------------------------------------------------- consumers
     uint32_t it = 0;
     bool dead = false;
     auto next_c = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
-    while (gen_next<PH>(gen, d, P, sc, next_c)) {
+    while (gen_next<PH, UPI>(gen, d, P, sc, next_c)) {
       const Proj& pj = d.dn ? P.pd : P.pu;
-      const int bx = NXB == 2 ? (d.pidx & 1) : 0;
       const int be = d.pidx & 1;
-      warp_wait(&B.xfull[bx], (d.pidx / NXB) & 1, P, abort_flag, dead);
-      const uint8_t* xs_s = smem + Ly.xs + bx * Ly.xs_stride;
-      const float* xm_s = reinterpret_cast<const float*>(smem + Ly.xm + bx * Ly.xm_stride);
-      const uint16_t* xraw = reinterpret_cast<const uint16_t*>(d.dn ? P.h : P.x);
-      const int* prow = pdesc + 16 * bx;
-      float* ep = epi + be * 512;
+      float* ep = epi + be * (MAXR * 64 * UPI);
       const uint32_t eph = ((d.pidx >> 1) & 1) ^ 1;
-      if (d.dn) dispatch_pass<KIND, MAXR_D, true, C::COLS>(d.t, P, pj, ring, B, bx, be, eph, d.pidx >= 2, abort_flag,
-                                                           xs_s, xm_s, prow, xraw, d.real, it, dead, ep);
-      else dispatch_pass<KIND, MAXR_U, false, C::COLS>(d.t, P, pj, ring, B, bx, be, eph, d.pidx >= 2, abort_flag,
-                                                       xs_s, xm_s, prow, xraw, d.real, it, dead, ep);
+      if (d.dn) dispatch_pass<KIND, MAXR_D, true, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag,
+                                                       r_prow, d.pos, d.real, it, dead, ep);
+      else dispatch_pass<KIND, MAXR_U, false, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow,
+                                                   d.pos, d.real, it, dead, ep);
     }
   }
 }
@@ -1357,23 +1426,22 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT)
 std::mutex& rows_mutex();
 int dev_sms(int* sms, size_t* optin);
 
-// Shared-memory shape and blocks per SM, chosen once per (device, kernel instance, shape) and
+// Ring depth and blocks per SM, chosen once per (device, kernel instance, route size) and
 // cached, so that steady-state launches (and launches under stream capture) issue only the
-// kernel. Candidates: activation rows by bulk copy or by global loads, one or two activation
-// buffers (two let the next pass stage while this one runs), ring depth 2..6. The pick keeps
-// the most weight bytes in flight per SM (resident blocks x ring stages, up to 6 a block),
-// then prefers two buffers, then bulk-copied rows, then more resident blocks.
+// kernel: about UNITS_IN_FLIGHT packed-unit stages in flight per SM (resident CTAs x slots x
+// units per slot), then more resident CTAs.
 template <int KIND, int MAXR_U, int MAXR_D, int PH>
 int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
   using Sh = RowsShape<KIND, MAXR_U, MAXR_D, PH>;
+  using SR = SlotRow<KIND>;
   constexpr int MAXR = Sh::MAXR;
-  constexpr int NT = Sh::C::NT;
+  constexpr int NT = Sh::C::NT, UPI = Sh::C::UPI;
   int sms;
   size_t optin;
   int rc = dev_sms(&sms, &optin);
   if (rc) return rc;
   auto kern = rows_kernel<KIND, MAXR_U, MAXR_D, PH>;
-  struct Entry { int key_gb, key_route, key_raw, nst, nxb, use_raw, nb; size_t smem; };
+  struct Entry { int key_route, nst, nb; size_t smem; };
   static Entry cache[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TFX_ECUDA;
@@ -1381,40 +1449,36 @@ int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
   {
     std::lock_guard<std::mutex> lk(rows_mutex());
     ent = cache[dev];
-    if (ent.nb == 0 || ent.key_gb != P.gbmax || ent.key_route != P.route_ints || ent.key_raw != P.raw_row) {
+    if (ent.nb == 0 || ent.key_route != P.route_ints) {
       RowsParams q = P;
-      q.nstage = 6;
-      q.nxb = 2;
-      q.use_raw = 1;
-      const size_t smax = (size_t)layout_of(q, MAXR).total;
+      q.nstage = MAX_NSTAGE;
+      const size_t smax = (size_t)layout_of(q, MAXR, UPI, SR::ACT).total;
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)min(smax, optin)) != cudaSuccess)
         return TFX_ELAUNCH;
       Entry best = {};
       long best_score = -1;
-      for (int raw = 0; raw <= 1; ++raw)
-        for (int nxb = 1; nxb <= 2; ++nxb)
-          for (int nst = 2; nst <= 6; ++nst) {
-            q.nstage = nst;
-            q.use_raw = raw;
-            q.nxb = nxb;
-            const size_t sm = (size_t)layout_of(q, MAXR).total;
-            if (sm > optin) continue;
-            int nb = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NT, sm) != cudaSuccess) return TFX_ELAUNCH;
-            if (nb < 1) continue;
-            const long score = (long)min(nb * nst, 8) * 1000 + (nxb == 2 ? 100 : 0) + raw * 10 + nb;
-            if (score > best_score) {
-              best_score = score;
-              best = Entry{P.gbmax, P.route_ints, P.raw_row, nst, nxb, raw, nb, sm};
-            }
-          }
+      for (int nst = 2; nst <= MAX_NSTAGE; ++nst) {
+        q.nstage = nst;
+        const size_t sm = (size_t)layout_of(q, MAXR, UPI, SR::ACT).total;
+        if (sm > optin) break;
+        int nb = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NT, sm) != cudaSuccess) return TFX_ELAUNCH;
+        if (nb < 1) break;
+        // about 8 packed units in flight per SM keep HBM busy; more only lengthen the queues
+        // that the gate/up -> down dependency waits in (measured: 5 slots a CTA were 8% slower
+        // than 4 on the one-row layer)
+        const int units = nb * nst * UPI;
+        const long score = (units <= UNITS_IN_FLIGHT ? units * 100 : UNITS_IN_FLIGHT * 100 - (units - UNITS_IN_FLIGHT) * 10) + nb;
+        if (score > best_score) {
+          best_score = score;
+          best = Entry{P.route_ints, nst, nb, sm};
+        }
+      }
       if (best_score < 0) return TFX_EUNSUPPORTED;
       ent = best;
       cache[dev] = ent;
     }
   }
-  P.use_raw = ent.use_raw;
-  P.nxb = ent.nxb;
   P.nstage = ent.nst;
   const int grid = min(max_items, ent.nb * sms);
   if (grid < 1) return TFX_OK;
