@@ -96,7 +96,7 @@ def tensor_peak_fp8():
     return 2.0 * FALLBACK_BF16_TFLOPS, "fallback bf16 x 2"
 
 
-def kernel_hash(files=("tfx_rows.cu", "tfx_common.cuh")):
+def kernel_hash(files=("tfx_rows.cu", "tfx_rows.cuh", "tfx_common.cuh")):
     h = hashlib.sha256()
     for n in files:
         with open(os.path.join(ROOT, "moe_routed_expert_major_gb300", "csrc", n), "rb") as f:
@@ -104,7 +104,7 @@ def kernel_hash(files=("tfx_rows.cu", "tfx_common.cuh")):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name, files=("tfx_rows.cu", "tfx_common.cuh")):
+def profiled_traffic(name, files=("tfx_rows.cu", "tfx_rows.cuh", "tfx_common.cuh")):
     """dram bytes (read + write) per launch of the timed kernel from the committed ncu summary
     profiles/<name>.md, if it was taken on the current kernel source; else None."""
     p = os.path.join(ROOT, "profiles", "%s.md" % name)

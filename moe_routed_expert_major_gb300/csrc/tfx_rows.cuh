@@ -158,8 +158,13 @@ __device__ __forceinline__ int tier_of(int left, int cap, int mode, bool down) {
 
 // Byte offset, in a converted activation row of one stage, of local group g (0..15) and
 // 8-element chunk tc: chunk ((g/8)*4 + tc)*8 + g%8 of 16 bytes, so the eight lanes that read
-// one chunk index of eight consecutive groups touch 128 consecutive bytes (fp32 rows: twice).
+// one chunk index of eight consecutive groups touch 128 consecutive bytes. fp32 rows split each
+// chunk into halves hf of four values: 16-byte piece (((g/8)*4 + tc)*2 + hf)*8 + g%8, so that
+// each 16-byte read of eight lanes is again 128 consecutive bytes.
 __device__ __forceinline__ int xoff(int g, int tc) { return ((((g >> 3) * 4 + tc) * 8 + (g & 7)) << 4); }
+__device__ __forceinline__ int xoff32(int g, int tc, int hf) {
+  return (((((g >> 3) * 4 + tc) * 2 + hf) * 8 + (g & 7)) << 4);
+}
 
 // Exact fp32 chain for a bf16 group whose values do not fit f16 after the shift: the
 // group's codes are decoded again, and each product of an E2M1 value with the bf16 value read
@@ -376,9 +381,8 @@ __device__ __forceinline__ void stage_store(const StageRegs<KIND, MODE, MR>& R_,
         o1.y = v.z & 0xFFFF0000u;
         o1.z = v.w << 16;
         o1.w = v.w & 0xFFFF0000u;
-        uint4* dst = reinterpret_cast<uint4*>(ar + 2 * xoff(g, tc));
-        dst[0] = o0;
-        dst[1] = o1;
+        *reinterpret_cast<uint4*>(ar + xoff32(g, tc, 0)) = o0;
+        *reinterpret_cast<uint4*>(ar + xoff32(g, tc, 1)) = o1;
       }
       if (lane < GPS) xm[r * xm_stride + lane] = 1.0f;
     }
@@ -664,7 +668,7 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, co
         if (X32) {
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
-            const float4 xa = *reinterpret_cast<const float4*>(xp + 16 * hf);
+            const float4 xa = *reinterpret_cast<const float4*>(xp + 128 * hf);
 #pragma unroll
             for (int ii = 0; ii < 2; ++ii) {
               const int i = 2 * hf + ii;
@@ -698,7 +702,7 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, co
       const uint8_t* sb = ring + (size_t)slot * Ly.slot;
       const uint8_t* tile = sb + uu * STAGE_B;
       const uint8_t* sc = tile + TROWS * CODE_B;
-      const uint8_t* xa_base = sb + Ly.act + XB * j * 16;
+      const uint8_t* xa_base = sb + Ly.act + 16 * j;  // f16 chunks: xoff; fp32 halves: xoff32
       const float* xm = reinterpret_cast<const float*>(sb + Ly.xm);
       const uint4 cA0 = *reinterpret_cast<const uint4*>(tile + rr * CODE_B + 16 * j);
       const uint4 cA1 = *reinterpret_cast<const uint4*>(tile + (32 + rr) * CODE_B + 16 * j);
@@ -743,8 +747,8 @@ __device__ __forceinline__ void run_pass(const RowsParams& P, const Proj& pj, co
             if (X32) {
 #pragma unroll
               for (int hf = 0; hf < 2; ++hf) {  // four values of each group at a time
-                const float4 xa = *reinterpret_cast<const float4*>(xp + 16 * hf);
-                const float4 xb = *reinterpret_cast<const float4*>(xp + 1024 + 16 * hf);
+                const float4 xa = *reinterpret_cast<const float4*>(xp + 128 * hf);
+                const float4 xb = *reinterpret_cast<const float4*>(xp + 1024 + 128 * hf);
 #pragma unroll
                 for (int ii = 0; ii < 2; ++ii) {
                   const int i = 2 * hf + ii;
