@@ -60,6 +60,8 @@ constexpr int MAX_PASS_U = 8;                    // longest gate/up pass
 constexpr int MAX_PASS_D = 4;                    // longest down pass
 constexpr int QD = 4;                            // claimed-item queue depth (fused)
 constexpr int UNITS_IN_FLIGHT = 8;               // weight stages (of one packed unit) in flight per SM
+constexpr int GU_SPLIT = 8;                      // gate/up passes of this many (row, unit) items or more:
+                                                 // epilogue run by the consumer warps
 
 enum { PH_UPC = 1, PH_DOWN = 2, PH_FUSED = 3 };
 
@@ -121,7 +123,7 @@ __host__ __device__ inline int fused_route_ints(int E, int R, int k, int nw) {
 }
 
 // ---------------------------------------------------------------- shared-memory layout
-// bars: full[8], empty[8], efull[2], eempty[2], qfull[4], qempty[4]; ctrl: abort flag and the
+// bars: full[8], empty[8], efull[2], eempty[2], qfull[4], qempty[4], hdone[2]; ctrl: abort flag and the
 // claimed-item queue; epi: two result buffers [maxr][64 upi] fp32; route: the fused launch's
 // lists; then the ring of slots: [upi weight stages | maxr converted activation rows | maxr x 16
 // group multipliers].
@@ -578,6 +580,7 @@ struct Bars {
   uint64_t *full, *empty;   // ring slots: producer (weights landed) and stager (activations
                             // converted) -> consumers; consumers -> producer and stager
   uint64_t *efull, *eempty; // result buffers: consumers -> epilogue, epilogue -> consumers
+  uint64_t* hdone;           // gate/up: the consumers' h stores of a pass are out -> epilogue
 };
 
 // Bounded wait whose outcome is uniform across the calling warp; on failure the block is
@@ -852,63 +855,76 @@ struct HPass {
   int pair[8];
 };
 
-// Epilogue warp: the epilogue of one pass, from result buffer epi; the pass's (row, unit)
-// items are taken four at a time, so that their latency chains overlap. Gate/up: SwiGLU, the
-// activation quantiser and h (+ debug copies); fused launches publish a finished gate/up unit.
-// Down: the expert outputs d; fused launches then count each (row, 64-output block) written,
-// with one fence for the whole pass, and combine the blocks whose last slot this pass wrote.
-template <int KIND, int PH, int UPI>
+// The gate/up epilogue of items i0, i0 + DI, ... of a pass (item i: row i / nu, unit i % nu),
+// by the calling warp, four items at a time so that their latency chains overlap: SwiGLU, the
+// activation quantiser and h (+ debug copies), from result buffer epi.
+template <int KIND, int UPI, int DI>
+__device__ __forceinline__ void gu_items(const RowsParams& P, const HPass& q, const float* epi, int i0) {
+  const int lane = threadIdx.x & 31;
+  const int n_items = q.real * q.nu;
+  const int I = P.I;
+  for (int ib = i0; ib < n_items; ib += 4 * DI) {
+    float g[4], u[4], hv[4];
+    int pp[4], nn[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int i = ib + c * DI;
+      if (i >= n_items) break;
+      const int r = i / q.nu, uu = i - r * q.nu;
+      const float* er = epi + r * 64 * UPI + 64 * uu;
+      pp[c] = q.pair[r];
+      nn[c] = 32 * (q.ub + uu) + lane;
+      g[c] = er[lane];
+      u[c] = er[32 + lane];
+      const float den = __fadd_rn(1.0f, expf(-g[c]));
+      hv[c] = __fmul_rn(__fdiv_rn(g[c], den), u[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (ib + c * DI >= n_items) break;
+      const size_t p = (size_t)pp[c];
+      if (P.gu_dbg) {
+        P.gu_dbg[p * 2 * I + nn[c]] = g[c];
+        P.gu_dbg[p * 2 * I + I + nn[c]] = u[c];
+      }
+      if (P.h_dbg) P.h_dbg[p * I + nn[c]] = hv[c];
+      if (KIND == TFX_ACT_E4M3) {
+        const bool bad = __any_sync(0xffffffffu, isnan(hv[c]) || isinf(hv[c]));
+        const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));
+        uint32_t sc;
+        if (bad) sc = 255u;
+        else if (amax_b == 0u) sc = 127u;
+        else {
+          const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
+          sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
+        }
+        const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv[c], e8m0_recip_f32(sc)));
+        static_cast<uint8_t*>(P.h)[p * I + nn[c]] = (uint8_t)code;
+        if (lane == 0) P.hs[p * (I / 32) + (nn[c] >> 5)] = (uint8_t)sc;
+      } else {
+        static_cast<__nv_bfloat16*>(P.h)[p * I + nn[c]] = __float2bfloat16_rn(hv[c]);
+      }
+    }
+  }
+}
+
+// Epilogue warp: the epilogue of one pass. Gate/up: in instances whose passes can reach GU_SPLIT
+// items (CSPLIT), such passes were run by the consumer warps themselves and this warp waits on
+// hdone until they are through (their h stores out); other passes it runs here, from result
+// buffer epi. It then frees the buffer and, in fused launches, publishes a finished gate/up unit
+// (a release fence, then the expert's counter). Down: from result buffer epi, the expert outputs d; fused launches then count each
+// (row, 64-output block) written, with one fence for the whole pass, and combine the blocks
+// whose last slot this pass wrote.
+template <int KIND, int PH, int UPI, bool CSPLIT>
 __device__ void helper_epilogue(const RowsParams& P, const HPass& q, const Bars& B, const float* epi,
                                 const int* r_prow, const int* r_pslot, const int* r_rowcnt, int32_t* done_upc,
                                 int32_t* slots_done, volatile int* abort_flag, bool& dead) {
   const int lane = threadIdx.x & 31;
   const int be = q.pidx & 1;
-  warp_wait(&B.efull[be], (q.pidx >> 1) & 1, P, abort_flag, dead);
+  warp_wait(q.dn || !CSPLIT ? &B.efull[be] : &B.hdone[be], (q.pidx >> 1) & 1, P, abort_flag, dead);
   const int n_items = q.real * q.nu;  // item i: row i / nu, unit i % nu
-  if (!dead && !q.dn) {
-    const int I = P.I;
-    for (int i0 = 0; i0 < n_items; i0 += 4) {
-      float g[4], u[4], hv[4];
-      int pp[4], nn[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (i0 + c >= n_items) break;
-        const int i = i0 + c, r = i / q.nu, uu = i - r * q.nu;
-        const float* er = epi + r * 64 * UPI + 64 * uu;
-        pp[c] = q.pair[r];
-        nn[c] = 32 * (q.ub + uu) + lane;
-        g[c] = er[lane];
-        u[c] = er[32 + lane];
-        const float den = __fadd_rn(1.0f, expf(-g[c]));
-        hv[c] = __fmul_rn(__fdiv_rn(g[c], den), u[c]);
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (i0 + c >= n_items) break;
-        const size_t p = (size_t)pp[c];
-        if (P.gu_dbg) {
-          P.gu_dbg[p * 2 * I + nn[c]] = g[c];
-          P.gu_dbg[p * 2 * I + I + nn[c]] = u[c];
-        }
-        if (P.h_dbg) P.h_dbg[p * I + nn[c]] = hv[c];
-        if (KIND == TFX_ACT_E4M3) {
-          const bool bad = __any_sync(0xffffffffu, isnan(hv[c]) || isinf(hv[c]));
-          const uint32_t amax_b = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv[c])));
-          uint32_t sc;
-          if (bad) sc = 255u;
-          else if (amax_b == 0u) sc = 127u;
-          else {
-            const int e2 = amax_b >= 0x00800000u ? (int)(amax_b >> 23) - 127 : (31 - __clz((int)amax_b)) - 149;
-            sc = (uint32_t)min(max(e2 - 8 + 127, 0), 254);
-          }
-          const uint32_t code = bad ? 0x7Fu : f32_to_e4m3(__fmul_rn(hv[c], e8m0_recip_f32(sc)));
-          static_cast<uint8_t*>(P.h)[p * I + nn[c]] = (uint8_t)code;
-          if (lane == 0) P.hs[p * (I / 32) + (nn[c] >> 5)] = (uint8_t)sc;
-        } else {
-          static_cast<__nv_bfloat16*>(P.h)[p * I + nn[c]] = __float2bfloat16_rn(hv[c]);
-        }
-      }
-    }
+  if (!q.dn) {
+    if (!dead && (!CSPLIT || n_items < GU_SPLIT)) gu_items<KIND, UPI, 1>(P, q, epi, 0);
   } else if (!dead) {
     bool bad = false;
     for (int i = 0; i < n_items; ++i) {
@@ -1103,6 +1119,9 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
   constexpr int MAXR = Sh::MAXR;
   constexpr int NCW = C::NCW, NT = C::NT, UPI = C::UPI;
   constexpr int AB = KIND == TFX_ACT_E4M3 ? 1 : 2;  // activation bytes per element
+  // the 8-row instance (gate/up passes of up to 8 rows x 2 units): the consumers run the epilogues
+  // of passes of GU_SPLIT items or more (hdone handshake); measured slower at fewer rows
+  constexpr bool CSPLIT = (PH & PH_UPC) && MAXR_U >= 8 && MAXR_U * UPI >= GU_SPLIT;
   extern __shared__ __align__(128) uint8_t smem[];
   const Layout Ly = layout_of(P, MAXR, UPI, SR::ACT);
   Bars B;
@@ -1112,6 +1131,7 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
   B.eempty = B.efull + 2;
   uint64_t* qfull = B.eempty + 2;  // fused: claimed-item queue, producer -> stager, epilogue, consumers
   uint64_t* qempty = qfull + QD;   //        and back
+  B.hdone = qempty + QD;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Ly.ctrl);
   int* qid = reinterpret_cast<int*>(smem + Ly.ctrl + 16);    // [QD] claimed item ids
   float* epi = reinterpret_cast<float*>(smem + Ly.epi);      // [2][maxr][64 upi]
@@ -1134,6 +1154,7 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
       mbar_init(&qfull[b], 1);
       mbar_init(&qempty[b], NCW + 1 + C::NSTG);
     }
+    for (int b = 0; b < 2; ++b) mbar_init(&B.hdone[b], NCW);
     mbar_fence_init();
     *abort_flag = 0;
   }
@@ -1188,6 +1209,21 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
   int32_t* slots_done = PH == PH_FUSED ? P.scratch + 2 + 2 * P.E : nullptr;
   PassGen gen = {};
   PassDesc d;
+  // the epilogue's view of a pass
+  auto hpass_of = [&](const PassDesc& q) {
+    HPass hp;
+    hp.dn = q.dn;
+    hp.last = q.last;
+    hp.a = q.a;
+    const Proj& pj = q.dn ? P.pd : P.pu;
+    hp.ub = UPI * q.u;
+    hp.nu = min(UPI, pj.units - hp.ub);
+    hp.real = q.real;
+    hp.pidx = q.pidx;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) hp.pair[r] = q.pos + min(r, q.real - 1);
+    return hp;
+  };
   // rows of a pass: token rows (gate/up) or pair rows (down); padding repeats the last
   auto row_of = [&](const PassDesc& q, int r) {
     const int src = q.pos + min(r, q.real - 1);
@@ -1390,19 +1426,8 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
     // ---------------------------------------------------------------- epilogue
     bool dead = false;
     auto epilogue = [&](const PassDesc& q) {
-      HPass hp;
-      hp.dn = q.dn;
-      hp.last = q.last;
-      hp.a = q.a;
-      const Proj& pj = q.dn ? P.pd : P.pu;
-      hp.ub = UPI * q.u;
-      hp.nu = min(UPI, pj.units - hp.ub);
-      hp.real = q.real;
-      hp.pidx = q.pidx;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) hp.pair[r] = q.pos + min(r, q.real - 1);
-      helper_epilogue<KIND, PH, UPI>(P, hp, B, epi + (q.pidx & 1) * (MAXR * 64 * UPI), r_prow, r_pslot, r_rowcnt,
-                                     done_upc, slots_done, abort_flag, dead);
+      helper_epilogue<KIND, PH, UPI, CSPLIT>(P, hpass_of(q), B, epi + (q.pidx & 1) * (MAXR * 64 * UPI), r_prow, r_pslot,
+                                     r_rowcnt, done_upc, slots_done, abort_flag, dead);
     };
     auto next_e = [&]() { return PH == PH_FUSED ? next_popped() : next_static(); };
     PassDesc q;
@@ -1421,6 +1446,16 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
                                                        r_prow, d.pos, d.real, it, dead, ep);
       else dispatch_pass<KIND, MAXR_U, false, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow,
                                                    d.pos, d.real, it, dead, ep);
+      // gate/up passes of GU_SPLIT or more (row, unit) items: once every consumer warp's results
+      // are in the buffer, the consumers run the epilogue items themselves (a lone epilogue warp
+      // gets few issue slots beside them); smaller passes leave them to the epilogue warp
+      if constexpr (CSPLIT) {
+        if (!d.dn && d.real * min(UPI, pj.units - UPI * d.u) >= GU_SPLIT &&
+            warp_wait(&B.efull[be], (d.pidx >> 1) & 1, P, abort_flag, dead))
+          gu_items<KIND, UPI, NCW>(P, hpass_of(d), ep, warp);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&B.hdone[be]);
+      }
     }
   }
 }
