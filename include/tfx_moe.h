@@ -270,9 +270,10 @@ int tfx_xp_router_grouped(int32_t rows, int32_t n_logits, int32_t top_k, const f
  * must not overlap on the device. The CTAs of one launch wait on one another, so the launch
  * is cooperative (all CTAs resident at once; the runtime refuses it otherwise: TFX_ELAUNCH);
  * a wait that runs out sets TFX_ST_TIMEOUT.
- * Work is handed out one pass at a time, pass-major (every expert's first gate/up pass, then
- * the second passes, ..., then the down passes in the same order), so consecutive passes on one
- * CTA mostly share their activation rows.
+ * Work is handed out one (pass, packed units) item at a time, expert-major (every gate/up pass
+ * of the first active expert, then of the second, ..., then the down passes in the same order),
+ * so that the down items claimed first are those whose gate/up items were handed out first, and
+ * consecutive items on one CTA mostly share their activation rows.
  * Returns TFX_EUNSUPPORTED for R*k > 256. opts->max_pass applies to gate/up (1..8); the down
  * pass is the same capped at 4. */
 size_t tfx_xp_moe_rows_scratch_bytes(tfx_dims d, int32_t rows);

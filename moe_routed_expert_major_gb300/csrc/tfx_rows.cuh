@@ -31,9 +31,10 @@
 //   * the epilogue warp takes each pass's results (SwiGLU and the activation quantiser, or the
 //     expert outputs and, in the fused launch, the combine) while the consumers go on;
 //   * the fused layer launch (cooperative: all CTAs resident) computes the row lists in shared
-//     memory in every CTA and hands out work units of one pass each, pass-major: first every
-//     expert's first gate/up pass, then the second passes, ..., then the down passes in the
-//     same order (each waits, bounded, for its expert's gate/up units). Each (row, 64-output
+//     memory in every CTA and hands out work units of one pass each, expert-major: every
+//     gate/up pass of the first active expert, then of the second, ..., then the down passes in
+//     the same order (each waits, bounded, for its expert's gate/up units), so that the down
+//     units claimed first are those of the experts whose gate/up units were handed out first. Each (row, 64-output
 //     block) is combined in the CTA whose down unit completes the row's last slot. Completion
 //     counters live in caller scratch; each counter's last user returns it to zero.
 #pragma once
@@ -393,8 +394,8 @@ __device__ __forceinline__ void stage_store(const StageRegs<KIND, MODE, MR>& R_,
 
 // Row lists of a small launch, computed in shared memory (fused layer): per-pair expert (or -1
 // if left out), per-expert counts -> offsets, active experts, stable positions, per-row slot
-// counts; then the pass lists of both projections (pass-major: every expert's first pass, then
-// every second pass, ...). All NT threads take part. Ints used: fused_route_ints(E, R, k).
+// counts; then the pass lists of both projections (expert-major: the first active expert's
+// passes, then the second's, ...). All NT threads take part. Ints used: fused_route_ints(E, R, k).
 struct SRoute {
   int *offs, *prow, *pslot, *act, *rowcnt, *ev, *cnt, *nact;
   int *plist_u, *plist_d;  // pass lists: a | start << 10 | real << 18 | t << 22
@@ -539,35 +540,37 @@ __device__ void route_smem(const RowsParams& p, int* base, SRoute& rt, int tid) 
       __syncwarp();
     }
   } else if (warp == 1 || warp == 2) {
-    // Pass lists (warp 1: gate/up, warp 2: down), pass-major.
+    // Pass lists (warp 1: gate/up, warp 2: down), expert-major: a warp scan of the pass counts
+    // places each expert's passes.
     const bool down = warp == 2;
     const int cap = down ? p.cap_d : p.cap_u;
     int* list = down ? rt.plist_d : rt.plist_u;
     uint16_t* np = down ? rt.np_d : rt.np_u;
     const int na = *rt.nact;
-    int maxp = 0;
     for (int a = lane; a < na; a += 32) {
       const int e = rt.act[a];
-      const int v = passes_of(rt.offs[e + 1] - rt.offs[e], cap, p.tier_mode, down);
-      np[a] = (uint16_t)v;
-      maxp = max(maxp, v);
+      np[a] = (uint16_t)passes_of(rt.offs[e + 1] - rt.offs[e], cap, p.tier_mode, down);
     }
-    maxp = __reduce_max_sync(0xffffffffu, maxp);
     __syncwarp();
     int count = 0;
-    for (int b = 0; b < maxp; ++b) {
-      for (int a0 = 0; a0 < na; a0 += 32) {
-        const int a = a0 + lane;
-        const bool has = a < na && np[a] > b;
-        const unsigned m = __ballot_sync(0xffffffffu, has);
-        if (has) {
-          const int e = rt.act[a];
+    for (int a0 = 0; a0 < na; a0 += 32) {
+      const int a = a0 + lane;
+      const int v = a < na ? (int)np[a] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (a < na) {
+        const int e = rt.act[a];
+        for (int b = 0; b < v; ++b) {
           int start, real, t;
           pass_rows(rt.offs[e + 1] - rt.offs[e], b, cap, p.tier_mode, down, start, real, t);
-          list[count + __popc(m & ((1u << lane) - 1u))] = pack_pass(a, start, real, t);
+          list[count + incl - v + b] = pack_pass(a, start, real, t);
         }
-        count += __popc(m);
       }
+      count += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) rt.nlist[down ? 1 : 0] = count;
   }
@@ -1232,7 +1235,7 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
     return (row < 0 || row >= P.R) ? 0 : row;
   };
   // Separate launches stride over the items; the fused launch hands units out dynamically: the
-  // producer claims them from a global counter, in order (gate/up units pass-major, then down
+  // producer claims them from a global counter, in order (gate/up units expert-major, then down
   // units), and passes them to the other roles through a small queue.
   int static_next = blockIdx.x - (int)gridDim.x;
   uint32_t qpos = 0;
