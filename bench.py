@@ -176,6 +176,23 @@ SWEEP = ([("shared", R, "e4m3", "fused") for R in (2, 3, 4, 5, 8, 16)] +
          [("apart", R, "bf16", "fused") for R in (2, 4, 8, 16)] + [("chunk", 4096, "e4m3", "chunk")])
 
 
+def layer_bytes(H, I, R, k, n_distinct, e4m3):
+    """Algorithmic bytes of one layer: the distinct experts' weights once, the activations in, h
+    written and read back, the expert outputs written and read back by the combine, the ids and
+    weights, and y (bf16)."""
+    P = R * k
+    act_b = 1 if e4m3 else 2
+    x_b = R * H * act_b + (R * (H // 32) if e4m3 else 0)
+    h_b = P * I * act_b + (P * (I // 32) if e4m3 else 0)
+    return n_distinct * expert_bytes(H, I) + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
+
+
+def layer_fmas(H, I, R, k):
+    """Multiply-adds of the fp32 chains of one layer: one per weight per routed pair (gate, up
+    and down: 3 H I)."""
+    return R * k * 3 * H * I
+
+
 def fma_peak(sms, mhz):
     """fp32-chain multiply-adds per second: SMs x 128 fma lanes per clock x the SM clock."""
     return sms * 128 * mhz * 1e6
@@ -218,15 +235,8 @@ class Runner:
         self.buf = tfx_.alloc_layer(R, H, I, E, k, kind, dev, chunk=self.chunk)
         self.n_distinct = len(set(int(e) for e in inp["ids"].ravel()))
         self.wbytes = self.n_distinct * expert_bytes(H, I)
-        P = R * k
-        act_b = 1 if kind == synth.ACT_E4M3 else 2
-        x_b = R * H * act_b + (R * (H // 32) if kind == synth.ACT_E4M3 else 0)
-        h_b = P * I * act_b + (P * (I // 32) if kind == synth.ACT_E4M3 else 0)
-        # algorithmic bytes of one layer: the distinct experts' weights once, activations in, h
-        # written and read back, the expert outputs written and read back by the combine,
-        # ids/weights, and y
-        self.alg_bytes = self.wbytes + x_b + 2 * h_b + 2 * P * H * 4 + P * 8 + R * H * 2
-        self.fmas = P * 3 * H * I       # multiply-adds of the fp32 chains (one per weight per routed pair)
+        self.alg_bytes = layer_bytes(H, I, R, k, self.n_distinct, kind == synth.ACT_E4M3)
+        self.fmas = layer_fmas(H, I, R, k)
         self.flops = 2.0 * self.fmas    # the same as flops, for the tensor-core path
         self.launches = 1 if self.fused else (5 if self.chunk else 4)
         self.tfx = tfx_
