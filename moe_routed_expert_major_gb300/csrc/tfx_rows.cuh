@@ -1445,10 +1445,19 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
       const int be = d.pidx & 1;
       float* ep = epi + be * (MAXR * 64 * UPI);
       const uint32_t eph = ((d.pidx >> 1) & 1) ^ 1;
-      if (d.dn) dispatch_pass<KIND, MAXR_D, true, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag,
-                                                       r_prow, d.pos, d.real, it, dead, ep);
-      else dispatch_pass<KIND, MAXR_U, false, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow,
-                                                   d.pos, d.real, it, dead, ep);
+      if constexpr (KIND == TFX_ACT_E4M3 && MAXR_D <= MAXR_U) {
+        // E4M3 gate/up and down passes of up to MAXR_U rows are the same code (the down flag only
+        // matters to bf16): one inlined copy of it, for the instruction cache (measured: 0.3-3%
+        // faster layers)
+        dispatch_pass<KIND, MAXR_U, false, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow,
+                                                d.pos, d.real, it, dead, ep);
+      } else if (d.dn) {
+        dispatch_pass<KIND, MAXR_D, true, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow, d.pos,
+                                               d.real, it, dead, ep);
+      } else {
+        dispatch_pass<KIND, MAXR_U, false, UPI>(d.t, P, pj, smem, Ly, B, be, eph, d.pidx >= 2, abort_flag, r_prow,
+                                                d.pos, d.real, it, dead, ep);
+      }
       // gate/up passes of GU_SPLIT or more (row, unit) items: once every consumer warp's results
       // are in the buffer, the consumers run the epilogue items themselves (a lone epilogue warp
       // gets few issue slots beside them); smaller passes leave them to the epilogue warp
