@@ -1410,8 +1410,16 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
           }
         };
         if (KIND == TFX_ACT_E4M3) {
-          if (d.dn) run_stage(std::integral_constant<int, 0>(), std::true_type(), rw);
-          else run_stage(std::integral_constant<int, 0>(), std::false_type(), rw);
+          if constexpr (MAXR_U >= 8) {
+            // the 8-row instance stages x as it stages h (through L2): one copy of the staging
+            // code instead of two (measured: 3-4% faster shared 5-16 rows, 17% apart 16 rows;
+            // the smaller instances keep x in L1, one row 2% faster that way)
+            run_stage(std::integral_constant<int, 0>(), std::true_type(), rw);
+          } else if (d.dn) {
+            run_stage(std::integral_constant<int, 0>(), std::true_type(), rw);
+          } else {
+            run_stage(std::integral_constant<int, 0>(), std::false_type(), rw);
+          }
         } else if (d.dn) {
           int rwd[MAXR_D];
 #pragma unroll
