@@ -605,6 +605,22 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return ok;
 }
 
+// L2 policy for data read once: evicted before anything else, so that the kernel's code and
+// the data it reuses stay resident while the weight stream passes through.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// One-dimensional bulk copy global -> shared with an L2 cache policy (as bulk_g2s).
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
 // E8M0 code -> fp32 bits (those of e8m0_to_f32), a table read through L1 by the consumers.
 struct E8m0Table {
   uint32_t v[256];
@@ -1257,6 +1273,10 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
       uint32_t it = 0;
       bool stop = false;
       uint32_t claims = 0;
+      // every weight byte is read once a launch: evict it first, so that the code, the
+      // activations, h, d and the counters stay in L2 while 23 MB an expert stream through
+      // (measured: 0.4 us on the one-row layer, 2-4% on shared and apart layers)
+      const uint64_t wpol = l2_evict_first_policy();
       auto claim = [&]() {  // producer lane: claim a unit and publish it to the queue
         const int slot = claims % QD;
         int v = -1;
@@ -1321,7 +1341,8 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
           uint8_t* sb = ring + (size_t)slot * Ly.slot;
           mbar_arrive_expect_tx(&B.full[slot], (uint32_t)(nu * STAGE_B));
           for (int v = 0; v < nu; ++v)
-            bulk_g2s(sb + v * STAGE_B, src + (size_t)v * pj.unit_bytes + (size_t)s * STAGE_B, STAGE_B, &B.full[slot]);
+            bulk_g2s_hint(sb + v * STAGE_B, src + (size_t)v * pj.unit_bytes + (size_t)s * STAGE_B, STAGE_B, &B.full[slot],
+                          wpol);
           if (PH == PH_FUSED && (it + 1 >= (uint32_t)NST || s == pj.S - 1)) claim_pending();
         }
       }
