@@ -60,7 +60,7 @@ constexpr int FUSED_MAX_PAIRS = 256;
 constexpr int MAX_PASS_U = 8;                    // longest gate/up pass
 constexpr int MAX_PASS_D = 4;                    // longest down pass
 constexpr int QD = 4;                            // claimed-item queue depth (fused)
-constexpr int UNITS_IN_FLIGHT = 8;               // weight stages (of one packed unit) in flight per SM
+constexpr int UNITS_IN_FLIGHT = 6;               // weight stages (of one packed unit) in flight per SM
 constexpr int GU_SPLIT = 8;                      // gate/up passes of this many (row, unit) items or more:
                                                  // epilogue run by the consumer warps
 
@@ -1304,8 +1304,11 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
         return v;
       };
       // The queue runs one unit ahead of the producer, so the other roles learn of the next
-      // unit while the current one streams. The claim of that next unit is made once the
-      // current unit's first stages are on their way.
+      // unit while the current one streams. The next unit is claimed when the current unit's
+      // last stage is issued: the ring still holds that unit's queued stages while the claim
+      // returns, and the units left are handed to the CTAs that are closest to done. (Claimed
+      // at a unit's first stage, the one-row layer's second gate/up wave went at start-up to
+      // CTAs that finished their first unit up to 8 us apart: 4-5% slower.)
       int ahead = -2;
       bool pending = false;
       auto claim_pending = [&]() {
@@ -1343,7 +1346,7 @@ __global__ void __launch_bounds__(RowsShape<KIND, MAXR_U, MAXR_D, PH>::C::NT,
           for (int v = 0; v < nu; ++v)
             bulk_g2s_hint(sb + v * STAGE_B, src + (size_t)v * pj.unit_bytes + (size_t)s * STAGE_B, STAGE_B, &B.full[slot],
                           wpol);
-          if (PH == PH_FUSED && (it + 1 >= (uint32_t)NST || s == pj.S - 1)) claim_pending();
+          if (PH == PH_FUSED && s == pj.S - 1) claim_pending();
         }
       }
       if (PH == PH_FUSED) claim_pending();
@@ -1544,9 +1547,10 @@ int launch_rows(RowsParams P, int max_items, cudaStream_t st) {
         int nb = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, NT, sm) != cudaSuccess) return TFX_ELAUNCH;
         if (nb < 1) break;
-        // about 8 packed units in flight per SM keep HBM busy; more only lengthen the queues
-        // that the gate/up -> down dependency waits in (measured: 5 slots a CTA were 8% slower
-        // than 4 on the one-row layer)
+        // about 6 packed units in flight per SM keep HBM busy; more only lengthen the queues
+        // that the gate/up -> down dependency waits in (measured against 8: level on the
+        // one-row layer, 1-6% faster on shared-row layers of 2-16 rows and 0.4-2% on bf16
+        // layers of 4-16 rows apart, 3% slower on 2 rows apart)
         const int units = nb * nst * UPI;
         const long score = (units <= UNITS_IN_FLIGHT ? units * 100 : UNITS_IN_FLIGHT * 100 - (units - UNITS_IN_FLIGHT) * 10) + nb;
         if (score > best_score) {
