@@ -505,13 +505,18 @@ def run_ours(args):
                  ("xs", np.ascontiguousarray(inp["sx"]) if kind == synth.ACT_E4M3 else None),
                  ("ids", np.ascontiguousarray(inp["ids"])), ("w", np.ascontiguousarray(inp["w"]))]
         offs, tot = {}, 0
-        for name, a in parts:
-            if a is not None:
-                offs[name] = tot
-                tot = (tot + a.nbytes + 255) // 256 * 256
+        if main.fused:
+            # the host-buffer entry's own block layout: it then moves the four parts in one copy
+            lay, tot = tfx.tfx_xp_moe_rows_host_layout(d, R, kind)
+            offs = {"x": lay[0], "xs": lay[1], "ids": lay[2], "w": lay[3]}
+        else:
+            for name, a in parts:
+                if a is not None:
+                    offs[name] = tot
+                    tot = (tot + a.nbytes + 255) // 256 * 256
         hin = torch.zeros(tot, dtype=torch.uint8).pin_memory()
         din = torch.empty(tot, dtype=torch.uint8, device=dev)
-        dv = {}
+        dv, hv = {}, {}
         for name, a in parts:
             if a is None:
                 continue
@@ -520,19 +525,24 @@ def run_ours(args):
             tdt = {np.dtype(np.uint8): torch.uint8, np.dtype(np.int16): torch.int16, np.dtype(np.int32): torch.int32,
                    np.dtype(np.float32): torch.float32}[a.dtype]
             dv[name] = din[offs[name]:offs[name] + a.nbytes].view(tdt).view(a.shape)
+            hv[name] = hin[offs[name]:offs[name] + a.nbytes].view(tdt).view(a.shape)
         dx, dxs, dids, dwt = dv["x"], dv.get("xs"), dv["ids"], dv["w"]
+        if main.fused:
+            host_ws = torch.zeros(tfx.tfx_xp_moe_rows_host_ws_bytes(d, R, kind), dtype=torch.uint8, device=dev)
         hy = torch.empty(buf["y"].shape, dtype=buf["y"].dtype).pin_memory()
         h2d = tot
         d2h = hy.numel() * hy.element_size()
         Ke = max(K, min(2000, int(0.5e6 / max(1.0, 1000.0 * elapsed_ms / K)))) if not main.chunk else min(K, 20)
 
         def e2e_step(i):
-            din.copy_(hin, non_blocking=True)
             pk = packed[i % L]
             if main.fused:
-                tfx.tfx_xp_moe_rows(d, R, kind, pk, dx, dxs, dids, dwt, buf["route"], buf["h"], buf["h_scale"],
-                                    buf["out"], buf["y"], buf["scratch"], buf["status"])
-            elif main.chunk:
+                # one call: the inputs' copy, the layer and the copy of y, queued on the stream
+                tfx.tfx_xp_moe_rows_host(d, R, kind, pk, hv["x"], hv.get("xs"), hv["ids"], hv["w"], hy,
+                                         buf["status"], host_ws)
+                return
+            din.copy_(hin, non_blocking=True)
+            if main.chunk:
                 tfx.tfx_xp_route(d, R, dids, buf["route"], buf["status"])
                 tfx.tfx_xp_upc_chunk(d, R, kind, pk, dx, dxs, buf["route"], buf["h"], buf["h_scale"], buf["chunk_ws"],
                                      buf["status"])
@@ -557,8 +567,11 @@ def run_ours(args):
         torch.cuda.synchronize()
         e2e = {"value": round(1000.0 * a.elapsed_time(b) / Ke, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": Ke,
-               "how": "the public API (ctypes binding of libtfx_moe.so) launched from Python each step: one pinned "
-                      "H2D copy of the step's inputs, the layer, one D2H copy of y, back to back on one stream"}
+               "how": ("the public API's host-buffer entry (tfx_xp_moe_rows_host through the ctypes binding), one "
+                       "call from Python each step: one H2D copy of the step's inputs from pinned memory, the layer, "
+                       "one D2H copy of y to pinned memory, queued on one stream" if main.fused else
+                       "the public API (ctypes binding of libtfx_moe.so) launched from Python each step: one pinned "
+                       "H2D copy of the step's inputs, the layer, one D2H copy of y, back to back on one stream")}
 
     # ---------------------------------------------------------------- the rest of the metric
     hbm, hbm_src = peaks()

@@ -308,6 +308,40 @@ int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const ui
                             uint8_t* h_scale, float* out, uint16_t* y, float* y_f32_dbg, int32_t* status,
                             const tfx_rows_opts* opts, void* stream);
 
+/* The one-launch layer from host buffers (no counterpart on the pages: an interface for
+ * callers whose activations and routing sit in host memory, and the call that the end-to-end
+ * measurement makes). One call queues on `stream`, in order:
+ *   - the copy of the inputs to the device (x, x_scale, ids and topk_w, laid out as for
+ *     tfx_xp_moe_rows; x_scale is ignored for bf16 activations);
+ *   - the layer, exactly as tfx_xp_moe_rows (same results, bit for bit);
+ *   - the copy of y (bf16 [R][H]) to y_host and, if status_host is not NULL, of the status
+ *     word to status_host.
+ * It returns once they are queued. The host buffers must stay valid, and y_host and status_host
+ * unread, until the stream has passed them. With pinned (page-locked) host memory the copies
+ * are asynchronous; with pageable memory the runtime waits for each copy on the host.
+ * One copy moves all four inputs when they lie back to back in one host block. That is when
+ * x_scale_host, ids_host and topk_w_host sit at the byte offsets from x_host that
+ * tfx_xp_moe_rows_host_layout gives (offsets[0..3], 16-byte aligned; in_bytes is the block's
+ * size). Otherwise each input is copied on its own.
+ * ws: tfx_xp_moe_rows_host_ws_bytes(d, R, act_kind) bytes of device memory, 256-byte aligned,
+ *   owned by the caller. It holds the scratch counters (zero before the first call, as for
+ *   tfx_xp_moe_rows) and the device copies of the inputs, row lists, h, out and y. Calls
+ *   sharing one ws must not overlap on the device.
+ * status: an int32 on the device that the layer ORs its flags into, as for tfx_xp_moe_rows.
+ * packed: the device copy of the packed weights (tfx_xp_pack).
+ * Returns TFX_EUNSUPPORTED for R*k > 256; TFX_EINVAL for bad sizes or kind, a ws that is NULL,
+ * misaligned or too small, a NULL host pointer (rows > 0) or any argument that tfx_xp_moe_rows
+ * refuses; all checks come before anything is queued. Returns TFX_ELAUNCH if a copy or the
+ * launch cannot be queued. rows = 0 queues nothing.
+ * tfx_xp_moe_rows_host_ws_bytes returns 0 for bad sizes or kind, or for R*k > 256;
+ * tfx_xp_moe_rows_host_layout returns TFX_EINVAL for those or NULL outputs. */
+size_t tfx_xp_moe_rows_host_ws_bytes(tfx_dims d, int32_t rows, int32_t act_kind);
+int tfx_xp_moe_rows_host_layout(tfx_dims d, int32_t rows, int32_t act_kind, size_t* offsets, size_t* in_bytes);
+int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed, const void* x_host,
+                         const uint8_t* x_scale_host, const int32_t* ids_host, const float* topk_w_host,
+                         uint16_t* y_host, int32_t* status, int32_t* status_host, void* ws, size_t ws_bytes,
+                         const tfx_rows_opts* opts, void* stream);
+
 /* ---------------------------------------------------------------- combine
  * The routing-weighted sum of a row's expert outputs, whose bf16 result "Receipt > Kernel
  * contract" of the same page checks per row (the combine output, bit-equal alone or with

@@ -287,3 +287,120 @@ extern "C" int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kin
   P.scratch = scratch;
   return moe_rows_launch(P, act_kind, max_items, stream);
 }
+
+// ------------------------------------------------------------------------------ host-buffer entry
+// The one-launch layer from host buffers: the inputs' copy to the device, the layer and the
+// copy of y back, queued on one stream by one call, with every device buffer carved from one
+// workspace.
+namespace tfx {
+
+struct HostLayout {
+  size_t in[4], in_bytes;  // x, x_scale, ids, topk_w within one input block (16-byte aligned)
+  size_t scratch, inputs, offs, prow, pslot, act, nact, h, hs, out, y, total;  // within ws
+};
+
+static size_t up16(size_t v) { return (v + 15) & ~(size_t)15; }
+static size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+static bool host_layout(tfx_dims d, int32_t rows, int32_t kind, HostLayout& L) {
+  if (!dims_ok(d) || rows < 0 || (kind != TFX_ACT_E4M3 && kind != TFX_ACT_BF16)) return false;
+  if ((int64_t)rows * d.top_k > FUSED_MAX_PAIRS) return false;
+  const size_t R = (size_t)rows, H = (size_t)d.hidden, I = (size_t)d.inter, E = (size_t)d.n_experts;
+  const size_t Pn = R * (size_t)d.top_k;
+  const bool e4 = kind == TFX_ACT_E4M3;
+  L.in[0] = 0;
+  L.in[1] = up16(R * H * (e4 ? 1 : 2));
+  L.in[2] = up16(L.in[1] + (e4 ? R * H / 32 : 0));
+  L.in[3] = up16(L.in[2] + Pn * sizeof(int32_t));
+  L.in_bytes = L.in[3] + Pn * sizeof(float);
+  size_t o = 0;
+  auto put = [&](size_t bytes) {
+    const size_t at = o;
+    o = up256(o + bytes);
+    return at;
+  };
+  L.scratch = put(tfx_xp_moe_rows_scratch_bytes(d, rows));
+  L.inputs = put(L.in_bytes);
+  L.offs = put((E + 1) * sizeof(int32_t));
+  L.prow = put(Pn * sizeof(int32_t));
+  L.pslot = put(Pn * sizeof(int32_t));
+  L.act = put(E * sizeof(int32_t));
+  L.nact = put(sizeof(int32_t));
+  L.h = put(Pn * I * (e4 ? 1 : 2));
+  L.hs = put(e4 ? Pn * I / 32 : 0);
+  L.out = put(Pn * H * sizeof(float));
+  L.y = put(R * H * sizeof(uint16_t));
+  L.total = o;
+  return true;
+}
+
+}  // namespace tfx
+
+extern "C" size_t tfx_xp_moe_rows_host_ws_bytes(tfx_dims d, int32_t rows, int32_t act_kind) {
+  HostLayout L;
+  return host_layout(d, rows, act_kind, L) ? L.total : 0;
+}
+
+extern "C" int tfx_xp_moe_rows_host_layout(tfx_dims d, int32_t rows, int32_t act_kind, size_t* offsets,
+                                           size_t* in_bytes) {
+  HostLayout L;
+  if (!offsets || !in_bytes || !host_layout(d, rows, act_kind, L)) return TFX_EINVAL;
+  for (int i = 0; i < 4; ++i) offsets[i] = L.in[i];
+  *in_bytes = L.in_bytes;
+  return TFX_OK;
+}
+
+extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, const uint8_t* packed,
+                                    const void* x_host, const uint8_t* x_scale_host, const int32_t* ids_host,
+                                    const float* topk_w_host, uint16_t* y_host, int32_t* status,
+                                    int32_t* status_host, void* ws, size_t ws_bytes, const tfx_rows_opts* opts,
+                                    void* stream) {
+  HostLayout L;
+  if (dims_ok(d) && (int64_t)rows * d.top_k > FUSED_MAX_PAIRS) return TFX_EUNSUPPORTED;  // as tfx_xp_moe_rows
+  if (!host_layout(d, rows, act_kind, L)) return TFX_EINVAL;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) || ws_bytes < L.total) return TFX_EINVAL;
+  const bool e4 = act_kind == TFX_ACT_E4M3;
+  if (rows > 0 && (!x_host || (e4 && !x_scale_host) || !ids_host || !topk_w_host || !y_host)) return TFX_EINVAL;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  uint8_t* din = w8 + L.inputs;
+  RowsParams P;
+  int max_items = 0;
+  int rc = moe_rows_prepare(d, rows, act_kind, packed, din + L.in[0], e4 ? din + L.in[1] : nullptr,
+                            reinterpret_cast<const int32_t*>(din + L.in[2]),
+                            reinterpret_cast<const float*>(din + L.in[3]), reinterpret_cast<int32_t*>(w8 + L.offs),
+                            reinterpret_cast<int32_t*>(w8 + L.prow), reinterpret_cast<int32_t*>(w8 + L.pslot),
+                            reinterpret_cast<int32_t*>(w8 + L.act), reinterpret_cast<int32_t*>(w8 + L.nact),
+                            w8 + L.h, e4 ? w8 + L.hs : nullptr, reinterpret_cast<float*>(w8 + L.out),
+                            reinterpret_cast<uint16_t*>(w8 + L.y), nullptr, nullptr, nullptr,
+                            reinterpret_cast<int32_t*>(w8 + L.scratch), true, status, opts, P, max_items);
+  if (rc || rows == 0) return rc;  // every argument checked before anything is queued
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t R = (size_t)rows, H = (size_t)d.hidden, Pn = R * (size_t)d.top_k;
+  const uint8_t* xb = static_cast<const uint8_t*>(x_host);
+  auto h2d = [&](size_t off, const void* src, size_t n) {
+    return cudaMemcpyAsync(din + off, src, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  // inputs laid out back to back as tfx_xp_moe_rows_host_layout gives: one copy moves them all
+  const bool one_block = (!e4 || x_scale_host == xb + L.in[1]) &&
+                         reinterpret_cast<const uint8_t*>(ids_host) == xb + L.in[2] &&
+                         reinterpret_cast<const uint8_t*>(topk_w_host) == xb + L.in[3];
+  bool ok;
+  if (one_block) {
+    ok = h2d(0, xb, L.in_bytes);
+  } else {
+    ok = h2d(L.in[0], xb, R * H * (e4 ? 1 : 2)) && (!e4 || h2d(L.in[1], x_scale_host, R * H / 32)) &&
+         h2d(L.in[2], ids_host, Pn * sizeof(int32_t)) && h2d(L.in[3], topk_w_host, Pn * sizeof(float));
+  }
+  if (!ok) {
+    (void)cudaGetLastError();
+    return TFX_ELAUNCH;
+  }
+  rc = moe_rows_launch(P, act_kind, max_items, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(y_host, w8 + L.y, R * H * sizeof(uint16_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      (status_host && cudaMemcpyAsync(status_host, status, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)) {
+    (void)cudaGetLastError();
+    return TFX_ELAUNCH;
+  }
+  return TFX_OK;
+}

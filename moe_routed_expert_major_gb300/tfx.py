@@ -68,6 +68,11 @@ def load():
                                                _P, _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_moe_rows_noalloc": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                                        _P, _P, _P, _P, _P, ctypes.POINTER(RowsOpts), _P]),
+            "tfx_xp_moe_rows_host_ws_bytes": (ctypes.c_size_t, [Dims, _I32, _I32]),
+            "tfx_xp_moe_rows_host_layout": (ctypes.c_int, [Dims, _I32, _I32, ctypes.POINTER(ctypes.c_size_t),
+                                                           ctypes.POINTER(ctypes.c_size_t)]),
+            "tfx_xp_moe_rows_host": (ctypes.c_int, [Dims, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                    ctypes.c_size_t, ctypes.POINTER(RowsOpts), _P]),
             "tfx_xp_router": (ctypes.c_int, [_I32, _I32, _I32, _P, _I32, _I32, _P, _P, _P]),
             "tfx_xp_router_grouped": (ctypes.c_int, [_I32, _I32, _I32, _P, _P, _I32, _I32, ctypes.c_float, _I32,
                                                      _P, _P, _P]),
@@ -88,6 +93,17 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("tfx: tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tfx: tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hptr(t):
+    """Host tensor -> pointer (pinned memory keeps the copies asynchronous)."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("tfx: this argument is a host buffer")
     if not t.is_contiguous():
         raise ValueError("tfx: tensors must be contiguous")
     return ctypes.c_void_p(t.data_ptr())
@@ -195,6 +211,29 @@ def tfx_xp_moe_rows_noalloc(d, rows, kind, packed, x, x_scale, ids, topk_w, rt, 
                                           _ptr(rt["active"]), _ptr(rt["n_active"]), _ptr(h), _ptr(h_scale), _ptr(out),
                                           _ptr(y), _ptr(y_f32), _ptr(status), o, _stream()),
            "tfx_xp_moe_rows_noalloc")
+
+
+def tfx_xp_moe_rows_host_ws_bytes(d, rows, kind):
+    return int(load().tfx_xp_moe_rows_host_ws_bytes(d, rows, kind))
+
+
+def tfx_xp_moe_rows_host_layout(d, rows, kind):
+    """(byte offsets of x, x_scale, ids and topk_w in one host input block, the block's size)."""
+    off = (ctypes.c_size_t * 4)()
+    n = ctypes.c_size_t()
+    _check(load().tfx_xp_moe_rows_host_layout(d, rows, kind, off, ctypes.byref(n)), "tfx_xp_moe_rows_host_layout")
+    return [int(v) for v in off], int(n.value)
+
+
+def tfx_xp_moe_rows_host(d, rows, kind, packed, x_host, x_scale_host, ids_host, topk_w_host, y_host, status, ws,
+                         status_host=None, opts=None):
+    """The one-launch layer from host buffers: copy in, the layer, copy y (and the status) out, all
+    queued on the current stream. packed, status and ws live on the device; the rest on the host."""
+    o = ctypes.byref(opts) if opts is not None else None
+    _check(load().tfx_xp_moe_rows_host(d, rows, kind, _ptr(packed), _hptr(x_host), _hptr(x_scale_host),
+                                       _hptr(ids_host), _hptr(topk_w_host), _hptr(y_host), _ptr(status),
+                                       _hptr(status_host), _ptr(ws), ws.numel() * ws.element_size(), o, _stream()),
+           "tfx_xp_moe_rows_host")
 
 
 ROUTER_SOFTMAX = 0

@@ -108,6 +108,27 @@ def noalloc(lib):
                                      p, None, None) == 0  # no rows: nothing to do
 
 
+def host_entry(lib):
+    """The host-buffer layer checks every argument before it queues a copy. Each refused call
+    carries a second bad argument, so that one regressed check still queues nothing; R = 0
+    queues nothing."""
+    L = lib
+    d = tfx.dims(7168, 2048, 256, 8)
+    p = ctypes.c_void_p(256)  # never dereferenced: validation fails first
+    need = L.tfx_xp_moe_rows_host_ws_bytes(d, 1, tfx.ACT_E4M3)
+    assert need > 0
+    call = lambda dd=d, rows=1, kind=tfx.ACT_E4M3, y=p, status=p, ws=p, wsb=need: L.tfx_xp_moe_rows_host(
+        dd, rows, kind, p, p, p, p, p, y, status, None, ws, wsb, None, None)
+    assert call(kind=7, status=None) == -1                      # unknown kind
+    assert call(ws=ctypes.c_void_p(256 + 16), y=None) == -1     # ws not 256-byte aligned
+    assert call(wsb=need - 1, status=None) == -1                # ws too small
+    assert call(ws=None, y=None) == -1                          # no ws
+    assert call(y=None, status=None) == -1                      # no y_host
+    assert call(dd=tfx.dims(7168, 2048, 0, 8), status=None) == -1  # bad sizes
+    assert call(rows=33, status=None) == -2                     # 264 routed pairs: beyond the one-launch layer
+    assert call(rows=0) == 0                                    # nothing to do
+
+
 if __name__ == "__main__":
     lib = tfx.load()
     for name in sys.argv[1:]:

@@ -72,3 +72,31 @@ def test_router_entries_reject_before_launch(lib):
 
 def test_noalloc_refuses_before_touching_its_buffer(lib):
     run_without_device("noalloc")
+
+
+def test_host_entry_refuses_before_queueing(lib):
+    run_without_device("host_entry")
+
+
+def test_host_entry_layout_by_hand(lib):
+    """The host entry's input block and workspace, worked out from the widths: the decode layer
+    (H 7168, I 2048, 256 experts, top-8, one row, E4M3) and two bf16 rows."""
+    from moe_routed_expert_major_gb300 import tfx
+    d = tfx.dims(7168, 2048, 256, 8)
+    # x 7,168 B; its 224 scales from 7,168; 8 ids from 7,392 (7,392 is 16-aligned); 8 weights
+    # from 7,424
+    assert tfx.tfx_xp_moe_rows_host_layout(d, 1, tfx.ACT_E4M3) == ([0, 7168, 7392, 7424], 7456)
+    # each part at the next 256-byte boundary: counters 4 x (2 + 2 x 256 + 112) = 2,504 B,
+    # the inputs 7,456, offs 257 x 4, pair_row and pair_slot 32 each, active 1,024, n_active 4,
+    # h 8 x 2,048, its scales 8 x 64, out 8 x 7,168 x 4 and y 7,168 x 2
+    sizes = [2504, 7456, 1028, 32, 32, 1024, 4, 16384, 512, 229376, 14336]
+    total = 0
+    for b in sizes:
+        total = (total + b + 255) // 256 * 256
+    assert total == 273920
+    assert tfx.tfx_xp_moe_rows_host_ws_bytes(d, 1, tfx.ACT_E4M3) == total
+    # bf16: x is 2 x 7,168 x 2 B and has no scales, so ids and x_scale share an offset
+    assert tfx.tfx_xp_moe_rows_host_layout(d, 2, tfx.ACT_BF16) == ([0, 28672, 28672, 28736], 28800)
+    assert tfx.tfx_xp_moe_rows_host_ws_bytes(d, 33, tfx.ACT_E4M3) == 0  # beyond 256 pairs
+    assert tfx.tfx_xp_moe_rows_host_ws_bytes(d, 1, 7) == 0
+

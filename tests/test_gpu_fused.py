@@ -4,7 +4,7 @@ bit for bit against the fp32-chain oracle, h within the float64 bound and quanti
 oracle's rule, every final value within the float64 bound), and against the four separate
 launches (identical row lists, h, d and combine output bit for bit) on small and full-width
 layers, every pass-size setting and the routing/NaN matrix; its scratch returns to zero after
-every call."""
+every call. The host-buffer entry (tfx_xp_moe_rows_host) gives its y bit for bit."""
 import numpy as np
 import pytest
 
@@ -68,6 +68,58 @@ def test_fused_matrix_and_pass_sizes(kind):
         for tm in (0, 1, 2):
             fus, _ = gu.run_layer_fused(lay, packed, opts=tfx.opts_struct(max_pass=mp, tier_mode=tm))
             gu.assert_same_layer(fus, sep, lay)
+
+
+_TORCH_DT = {np.dtype(np.uint8): torch.uint8, np.dtype(np.int16): torch.int16, np.dtype(np.int32): torch.int32,
+             np.dtype(np.float32): torch.float32}
+
+
+def _host_inputs(lay, d, block):
+    """The layer's x, x_scale, ids and weights in pinned host memory: in one block at the host
+    entry's offsets (one copy), or in four buffers of their own (one copy each)."""
+    R = lay["ids"].shape[0]
+    x = lay["x"].view(np.int16) if lay["kind"] == synth.ACT_BF16 else lay["x"]
+    parts = [x, lay["sx"] if lay["kind"] == synth.ACT_E4M3 else None, lay["ids"].astype(np.int32),
+             lay["w"].astype(np.float32)]
+    parts = [None if a is None else np.ascontiguousarray(a) for a in parts]
+    if not block:
+        return [None if a is None else torch.from_numpy(a).pin_memory() for a in parts]
+    off, n = tfx.tfx_xp_moe_rows_host_layout(d, R, lay["kind"])
+    blk = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    views = []
+    for o, a in zip(off, parts):
+        if a is None:
+            views.append(None)
+            continue
+        v = blk[o:o + a.nbytes]
+        v.copy_(torch.from_numpy(a.reshape(-1).view(np.uint8)))
+        views.append(v.view(_TORCH_DT[a.dtype]).view(a.shape))
+    return views
+
+
+@pytest.mark.parametrize("kind,R,block", [(synth.ACT_E4M3, 1, True), (synth.ACT_E4M3, 5, False),
+                                          (synth.ACT_BF16, 3, True), (synth.ACT_BF16, 2, False)],
+                         ids=["e4m3-1-block", "e4m3-5-apart", "bf16-3-block", "bf16-2-apart"])
+def test_host_entry_equals_device_entry(kind, R, block):
+    """tfx_xp_moe_rows_host (inputs copied in, y copied out, one call) gives y bit for bit as
+    tfx_xp_moe_rows on the same inputs, twice on one workspace."""
+    cfg = synth.workload("tiny", kind=kind, seed=23, H=1088, I=96, E=16, k=4)
+    lay = synth.make_layer_numpy(cfg, R=R)
+    d = tfx.dims(lay["H"], lay["I"], lay["E"], 4)
+    packed = gu.pack(d, gu.device_weights_from_numpy(lay))
+    ref, _ = gu.run_layer_fused(lay, packed)
+    assert ref["status"] == 0
+    xh, xsh, idh, wh = _host_inputs(lay, d, block)
+    yh = torch.empty(R, lay["H"], dtype=torch.int16).pin_memory()
+    sth = torch.full((1,), -1, dtype=torch.int32).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(tfx.tfx_xp_moe_rows_host_ws_bytes(d, R, kind), dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace, its counters back at zero
+        yh.fill_(0x5A5A)
+        tfx.tfx_xp_moe_rows_host(d, R, kind, packed, xh, xsh, idh, wh, yh, status, ws, status_host=sth)
+        torch.cuda.synchronize()
+        assert int(sth[0]) == 0
+        assert np.array_equal(yh.numpy().view(np.uint16), ref["y"].view(np.uint16))
 
 
 def test_fused_invalid_ids():
