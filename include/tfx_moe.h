@@ -314,8 +314,10 @@ int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const ui
  *   - the copy of the inputs to the device (x, x_scale, ids and topk_w, laid out as for
  *     tfx_xp_moe_rows; x_scale is ignored for bf16 activations);
  *   - the layer, exactly as tfx_xp_moe_rows (same results, bit for bit);
- *   - the copy of y (bf16 [R][H]) to y_host and, if status_host is not NULL, of the status
- *     word to status_host.
+ *   - y (bf16 [R][H]) into y_host, and, if status_host is not NULL, a copy of the status word
+ *     to status_host. When y_host is pinned host memory that the device can address
+ *     (cudaPointerGetAttributes reports host memory with a device pointer), the layer's combine
+ *     stores y there itself; otherwise y is copied there after the layer.
  * It returns once they are queued. The host buffers must stay valid, and y_host and status_host
  * unread, until the stream has passed them. With pinned (page-locked) host memory the copies
  * are asynchronous; with pageable memory the runtime waits for each copy on the host.

@@ -363,6 +363,19 @@ extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, 
   if (rows > 0 && (!x_host || (e4 && !x_scale_host) || !ids_host || !topk_w_host || !y_host)) return TFX_EINVAL;
   uint8_t* w8 = static_cast<uint8_t*>(ws);
   uint8_t* din = w8 + L.inputs;
+  // y goes straight to y_host when the device can address it (pinned host memory, mapped into
+  // the device's address space): the combine's stores then replace the copy back
+  uint16_t* y_dev = reinterpret_cast<uint16_t*>(w8 + L.y);
+  bool y_direct = false;
+  if (rows > 0) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, y_host) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer) {
+      y_dev = static_cast<uint16_t*>(a.devicePointer);
+      y_direct = true;
+    } else {
+      (void)cudaGetLastError();
+    }
+  }
   RowsParams P;
   int max_items = 0;
   int rc = moe_rows_prepare(d, rows, act_kind, packed, din + L.in[0], e4 ? din + L.in[1] : nullptr,
@@ -371,7 +384,7 @@ extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, 
                             reinterpret_cast<int32_t*>(w8 + L.prow), reinterpret_cast<int32_t*>(w8 + L.pslot),
                             reinterpret_cast<int32_t*>(w8 + L.act), reinterpret_cast<int32_t*>(w8 + L.nact),
                             w8 + L.h, e4 ? w8 + L.hs : nullptr, reinterpret_cast<float*>(w8 + L.out),
-                            reinterpret_cast<uint16_t*>(w8 + L.y), nullptr, nullptr, nullptr,
+                            y_dev, nullptr, nullptr, nullptr,
                             reinterpret_cast<int32_t*>(w8 + L.scratch), true, status, opts, P, max_items);
   if (rc || rows == 0) return rc;  // every argument checked before anything is queued
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -397,7 +410,8 @@ extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, 
   }
   rc = moe_rows_launch(P, act_kind, max_items, stream);
   if (rc) return rc;
-  if (cudaMemcpyAsync(y_host, w8 + L.y, R * H * sizeof(uint16_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+  if ((!y_direct &&
+       cudaMemcpyAsync(y_host, w8 + L.y, R * H * sizeof(uint16_t), cudaMemcpyDeviceToHost, st) != cudaSuccess) ||
       (status_host && cudaMemcpyAsync(status_host, status, sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess)) {
     (void)cudaGetLastError();
     return TFX_ELAUNCH;

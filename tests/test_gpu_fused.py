@@ -97,12 +97,13 @@ def _host_inputs(lay, d, block):
     return views
 
 
-@pytest.mark.parametrize("kind,R,block", [(synth.ACT_E4M3, 1, True), (synth.ACT_E4M3, 5, False),
-                                          (synth.ACT_BF16, 3, True), (synth.ACT_BF16, 2, False)],
-                         ids=["e4m3-1-block", "e4m3-5-apart", "bf16-3-block", "bf16-2-apart"])
-def test_host_entry_equals_device_entry(kind, R, block):
-    """tfx_xp_moe_rows_host (inputs copied in, y copied out, one call) gives y bit for bit as
-    tfx_xp_moe_rows on the same inputs, twice on one workspace."""
+@pytest.mark.parametrize("kind,R,block,pinned_y", [(synth.ACT_E4M3, 1, True, True), (synth.ACT_E4M3, 5, False, False),
+                                                   (synth.ACT_BF16, 3, True, False), (synth.ACT_BF16, 2, False, True)],
+                         ids=["e4m3-1-block", "e4m3-5-apart-pageable-y", "bf16-3-block-pageable-y", "bf16-2-apart"])
+def test_host_entry_equals_device_entry(kind, R, block, pinned_y):
+    """tfx_xp_moe_rows_host (inputs copied in; y stored into pinned host memory by the layer, or
+    copied into pageable memory; one call) gives y bit for bit as tfx_xp_moe_rows on the same
+    inputs, twice on one workspace."""
     cfg = synth.workload("tiny", kind=kind, seed=23, H=1088, I=96, E=16, k=4)
     lay = synth.make_layer_numpy(cfg, R=R)
     d = tfx.dims(lay["H"], lay["I"], lay["E"], 4)
@@ -110,7 +111,9 @@ def test_host_entry_equals_device_entry(kind, R, block):
     ref, _ = gu.run_layer_fused(lay, packed)
     assert ref["status"] == 0
     xh, xsh, idh, wh = _host_inputs(lay, d, block)
-    yh = torch.empty(R, lay["H"], dtype=torch.int16).pin_memory()
+    yh = torch.empty(R, lay["H"], dtype=torch.int16)
+    if pinned_y:
+        yh = yh.pin_memory()
     sth = torch.full((1,), -1, dtype=torch.int32).pin_memory()
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     ws = torch.zeros(tfx.tfx_xp_moe_rows_host_ws_bytes(d, R, kind), dtype=torch.uint8, device="cuda")
