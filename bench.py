@@ -568,8 +568,9 @@ def run_ours(args):
         e2e = {"value": round(1000.0 * a.elapsed_time(b) / Ke, 3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": Ke,
                "how": ("the public API's host-buffer entry (tfx_xp_moe_rows_host through the ctypes binding), one "
-                       "call from Python each step: one H2D copy of the step's inputs from pinned memory, then the "
-                       "layer, whose combine stores y into pinned host memory, queued on one stream" if main.fused else
+                       "call from Python each step: the layer reads the step's inputs in place from pinned host "
+                       "memory (h2d bytes: those inputs) and its combine stores y into pinned host memory (d2h "
+                       "bytes: y), queued on one stream" if main.fused else
                        "the public API (ctypes binding of libtfx_moe.so) launched from Python each step: one pinned "
                        "H2D copy of the step's inputs, the layer, one D2H copy of y, back to back on one stream")}
 

@@ -311,18 +311,21 @@ int tfx_xp_moe_rows_noalloc(tfx_dims d, int32_t rows, int32_t act_kind, const ui
 /* The one-launch layer from host buffers (no counterpart on the pages: an interface for
  * callers whose activations and routing sit in host memory, and the call that the end-to-end
  * measurement makes). One call queues on `stream`, in order:
- *   - the copy of the inputs to the device (x, x_scale, ids and topk_w, laid out as for
- *     tfx_xp_moe_rows; x_scale is ignored for bf16 activations);
+ *   - the inputs' way to the device (x, x_scale, ids and topk_w, laid out as for
+ *     tfx_xp_moe_rows; x_scale is ignored for bf16 activations). When all of them are pinned
+ *     host memory that the device can address, and x is 16-byte aligned, the layer reads them
+ *     in place and nothing is copied. Otherwise they are copied into ws (see below);
  *   - the layer, exactly as tfx_xp_moe_rows (same results, bit for bit);
  *   - y (bf16 [R][H]) into y_host, and, if status_host is not NULL, a copy of the status word
  *     to status_host. When y_host is pinned host memory that the device can address
  *     (cudaPointerGetAttributes reports host memory with a device pointer), the layer's combine
  *     stores y there itself; otherwise y is copied there after the layer.
- * It returns once they are queued. The host buffers must stay valid, and y_host and status_host
- * unread, until the stream has passed them. With pinned (page-locked) host memory the copies
- * are asynchronous; with pageable memory the runtime waits for each copy on the host.
- * One copy moves all four inputs when they lie back to back in one host block. That is when
- * x_scale_host, ids_host and topk_w_host sit at the byte offsets from x_host that
+ * It returns once they are queued. The host buffers must stay valid, the inputs unchanged and
+ * y_host and status_host unread, until the stream has passed the layer and its copies. With
+ * pinned (page-locked) host memory nothing waits on the host; with pageable memory the runtime
+ * waits for each copy on the host.
+ * When the inputs are copied, one copy moves all four if they lie back to back in one host
+ * block: x_scale_host, ids_host and topk_w_host at the byte offsets from x_host that
  * tfx_xp_moe_rows_host_layout gives (offsets[0..3], 16-byte aligned; in_bytes is the block's
  * size). Otherwise each input is copied on its own.
  * ws: tfx_xp_moe_rows_host_ws_bytes(d, R, act_kind) bytes of device memory, 256-byte aligned,

@@ -365,22 +365,41 @@ extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, 
   uint8_t* din = w8 + L.inputs;
   // y goes straight to y_host when the device can address it (pinned host memory, mapped into
   // the device's address space): the combine's stores then replace the copy back
-  uint16_t* y_dev = reinterpret_cast<uint16_t*>(w8 + L.y);
-  bool y_direct = false;
-  if (rows > 0) {
+  auto device_view = [](const void* p) -> void* {  // p's device address, if it has one
     cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, y_host) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer) {
-      y_dev = static_cast<uint16_t*>(a.devicePointer);
+    if (p && cudaPointerGetAttributes(&a, p) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer)
+      return a.devicePointer;
+    (void)cudaGetLastError();
+    return nullptr;
+  };
+  uint16_t* y_dev = reinterpret_cast<uint16_t*>(w8 + L.y);
+  bool y_direct = false, in_place = false;
+  const void* xd = din + L.in[0];
+  const void* xsd = e4 ? din + L.in[1] : nullptr;
+  const void* idd = din + L.in[2];
+  const void* wd = din + L.in[3];
+  if (rows > 0) {
+    if (void* v = device_view(y_host)) {
+      y_dev = static_cast<uint16_t*>(v);
       y_direct = true;
-    } else {
-      (void)cudaGetLastError();
+    }
+    void* vx = device_view(x_host);
+    void* vxs = e4 ? device_view(x_scale_host) : nullptr;
+    void* vid = device_view(ids_host);
+    void* vw = device_view(topk_w_host);
+    if (vx && aligned16(vx) && (!e4 || vxs) && vid && vw) {
+      xd = vx;
+      xsd = vxs;
+      idd = vid;
+      wd = vw;
+      in_place = true;
     }
   }
   RowsParams P;
   int max_items = 0;
-  int rc = moe_rows_prepare(d, rows, act_kind, packed, din + L.in[0], e4 ? din + L.in[1] : nullptr,
-                            reinterpret_cast<const int32_t*>(din + L.in[2]),
-                            reinterpret_cast<const float*>(din + L.in[3]), reinterpret_cast<int32_t*>(w8 + L.offs),
+  int rc = moe_rows_prepare(d, rows, act_kind, packed, xd, static_cast<const uint8_t*>(xsd),
+                            static_cast<const int32_t*>(idd), static_cast<const float*>(wd),
+                            reinterpret_cast<int32_t*>(w8 + L.offs),
                             reinterpret_cast<int32_t*>(w8 + L.prow), reinterpret_cast<int32_t*>(w8 + L.pslot),
                             reinterpret_cast<int32_t*>(w8 + L.act), reinterpret_cast<int32_t*>(w8 + L.nact),
                             w8 + L.h, e4 ? w8 + L.hs : nullptr, reinterpret_cast<float*>(w8 + L.out),
@@ -397,8 +416,10 @@ extern "C" int tfx_xp_moe_rows_host(tfx_dims d, int32_t rows, int32_t act_kind, 
   const bool one_block = (!e4 || x_scale_host == xb + L.in[1]) &&
                          reinterpret_cast<const uint8_t*>(ids_host) == xb + L.in[2] &&
                          reinterpret_cast<const uint8_t*>(topk_w_host) == xb + L.in[3];
-  bool ok;
-  if (one_block) {
+  bool ok = true;
+  if (in_place) {
+    // the layer reads the inputs where they are
+  } else if (one_block) {
     ok = h2d(0, xb, L.in_bytes);
   } else {
     ok = h2d(L.in[0], xb, R * H * (e4 ? 1 : 2)) && (!e4 || h2d(L.in[1], x_scale_host, R * H / 32)) &&

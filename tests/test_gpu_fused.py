@@ -74,18 +74,20 @@ _TORCH_DT = {np.dtype(np.uint8): torch.uint8, np.dtype(np.int16): torch.int16, n
              np.dtype(np.float32): torch.float32}
 
 
-def _host_inputs(lay, d, block):
-    """The layer's x, x_scale, ids and weights in pinned host memory: in one block at the host
-    entry's offsets (one copy), or in four buffers of their own (one copy each)."""
+def _host_inputs(lay, d, block, pinned):
+    """The layer's x, x_scale, ids and weights in host memory, in one block at the host entry's
+    offsets or in four buffers of their own; pinned (the layer reads them in place) or pageable
+    (copied to the device: one copy for the block, else one each)."""
     R = lay["ids"].shape[0]
     x = lay["x"].view(np.int16) if lay["kind"] == synth.ACT_BF16 else lay["x"]
     parts = [x, lay["sx"] if lay["kind"] == synth.ACT_E4M3 else None, lay["ids"].astype(np.int32),
              lay["w"].astype(np.float32)]
     parts = [None if a is None else np.ascontiguousarray(a) for a in parts]
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
     if not block:
-        return [None if a is None else torch.from_numpy(a).pin_memory() for a in parts]
+        return [None if a is None else pin(torch.from_numpy(a)) for a in parts]
     off, n = tfx.tfx_xp_moe_rows_host_layout(d, R, lay["kind"])
-    blk = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    blk = pin(torch.zeros(n, dtype=torch.uint8))
     views = []
     for o, a in zip(off, parts):
         if a is None:
@@ -97,20 +99,22 @@ def _host_inputs(lay, d, block):
     return views
 
 
-@pytest.mark.parametrize("kind,R,block,pinned_y", [(synth.ACT_E4M3, 1, True, True), (synth.ACT_E4M3, 5, False, False),
-                                                   (synth.ACT_BF16, 3, True, False), (synth.ACT_BF16, 2, False, True)],
-                         ids=["e4m3-1-block", "e4m3-5-apart-pageable-y", "bf16-3-block-pageable-y", "bf16-2-apart"])
-def test_host_entry_equals_device_entry(kind, R, block, pinned_y):
-    """tfx_xp_moe_rows_host (inputs copied in; y stored into pinned host memory by the layer, or
-    copied into pageable memory; one call) gives y bit for bit as tfx_xp_moe_rows on the same
-    inputs, twice on one workspace."""
+@pytest.mark.parametrize("kind,R,block,pinned_in,pinned_y", [
+    (synth.ACT_E4M3, 1, True, True, True), (synth.ACT_E4M3, 5, False, False, False),
+    (synth.ACT_BF16, 3, True, False, True), (synth.ACT_BF16, 2, False, True, False)],
+    ids=["e4m3-1-in-place", "e4m3-5-four-copies", "bf16-3-one-copy", "bf16-2-in-place-y-copied"])
+def test_host_entry_equals_device_entry(kind, R, block, pinned_in, pinned_y):
+    """tfx_xp_moe_rows_host, one call: inputs read in place from pinned memory or copied from
+    pageable memory (one block or four buffers); y stored into pinned memory by the layer or
+    copied into pageable memory. Its y equals tfx_xp_moe_rows's bit for bit on the same inputs,
+    twice on one workspace."""
     cfg = synth.workload("tiny", kind=kind, seed=23, H=1088, I=96, E=16, k=4)
     lay = synth.make_layer_numpy(cfg, R=R)
     d = tfx.dims(lay["H"], lay["I"], lay["E"], 4)
     packed = gu.pack(d, gu.device_weights_from_numpy(lay))
     ref, _ = gu.run_layer_fused(lay, packed)
     assert ref["status"] == 0
-    xh, xsh, idh, wh = _host_inputs(lay, d, block)
+    xh, xsh, idh, wh = _host_inputs(lay, d, block, pinned_in)
     yh = torch.empty(R, lay["H"], dtype=torch.int16)
     if pinned_y:
         yh = yh.pin_memory()
